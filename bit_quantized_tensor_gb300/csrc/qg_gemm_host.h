@@ -1,0 +1,25 @@
+// Host-side helpers of the tcgen05 GEMM shared between translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "qg_internal.h"
+
+namespace qg {
+
+// Encodes a 2-D TMA map over a K-major matrix (rows x k_elems, row stride in
+// bytes) with the 128-byte swizzle and a box of box_k x box_rows elements.
+// fp16 selects 2-byte elements, otherwise 1-byte elements.
+int make_tmap_kmajor(CUtensorMap* map, bool fp16, const void* base, int64_t k_elems, int64_t rows,
+                     int64_t row_stride_bytes, int box_k, int box_rows);
+
+// fp16 tcgen05 GEMM with an fp16 epilogue: C = A . B^T (+ bias per column).
+// A: M x K (lda elements), B: N x K (ldb elements), C: M x N (ldc elements).
+int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, int64_t M, int64_t N,
+                    int64_t K, __half* C, int64_t ldc, const __half* bias, const Ctl& ctl,
+                    cudaStream_t stream);
+
+// Grid size for the elementwise grid-stride kernels (256 threads per block).
+int conv_grid(int dev, int64_t work_items);
+
+}  // namespace qg

@@ -1,0 +1,183 @@
+/*
+ * qgemm.h -- C ABI of the GB300 (sm_103a) quantized tensor-core GEMM library.
+ *
+ * Sources of the operations (web pages on the subject):
+ *  [L4]   "Hand-Written PTX Tensor-Core GEMM Kernels: A Multi-Precision Study
+ *          on NVIDIA L4" (arXiv 2608.10103), abstract: exact INT8 and INT4
+ *          GEMM and the FP16 GEMM they are compared with.
+ *  [SM75] "fused-int4-gemm-sm75" README: INT4 weight-only (W4A16) linear with
+ *          register-level dequantization and per-group scales (group 128).
+ *  [W4A4] "Warp-Specialized Kernel Implementation for W4A4 MatMul on Latest
+ *          GPU Architectures", section 1: Y = (Q(X).Q(W)^T) (.) scale + L(X) + b.
+ *
+ * Conventions shared by every call
+ *  - Matrix names follow the GEMM C = A . B, with A: M x K, B: K x N, C: M x N.
+ *    A / X is stored row-major (QG_ROW_MAJOR, K contiguous).  B / W is stored
+ *    K-major, i.e. column-major as a K x N matrix (QG_COL_MAJOR) which is the
+ *    same bytes as an N x K row-major matrix.  C / Y is row-major.  Other
+ *    layouts return QG_ERR_UNSUPPORTED.
+ *  - "s4p": two signed 4-bit values per byte along K; the LOW nibble holds the
+ *    even k, the HIGH nibble the odd k; each nibble is two's complement.
+ *  - fp16 data is IEEE binary16 passed as uint16_t bit patterns.
+ *  - Leading dimensions are in elements (in BYTES for s4p operands).
+ *  - Every pointer is a DEVICE pointer owned by the caller.  The library never
+ *    allocates, frees or synchronizes in these calls (qg_device_status is the
+ *    one call that synchronizes).  Scratch memory, where a call needs it, is
+ *    passed in as a workspace of at least qg_workspace_size() bytes.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  Calls are thread-safe.
+ *  - Any M, N >= 1.  Divisibility of K is stated per call.
+ *  - Alignment: every pointer 16-byte aligned; the leading dimension of every
+ *    INPUT matrix times its element size a multiple of 16 bytes; otherwise
+ *    QG_ERR_MISALIGNED.  Output leading dimensions only need ldc >= N (rows
+ *    that start 16-byte aligned are written with vector stores).
+ *  - Errors: argument errors are detected synchronously before any launch and
+ *    nothing is enqueued.  A launch failure returns QG_ERR_CUDA.  Kernels bound
+ *    every wait; a wait that runs out records QG_ERR_TIMEOUT in a device
+ *    status word that qg_device_status() reports.  No call traps or aborts.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad group/block/rank  */
+    QG_ERR_UNSUPPORTED = 2,  /* layout or shape this build does not handle    */
+    QG_ERR_MISALIGNED = 3,   /* pointer or leading dimension not 16B aligned  */
+    QG_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required    */
+    QG_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed             */
+    QG_ERR_TIMEOUT = 6       /* a device-side bounded wait ran out            */
+} qg_status;
+
+typedef enum { QG_ROW_MAJOR = 0, QG_COL_MAJOR = 1 } qg_layout;
+
+/* Operation ids for qg_workspace_size. */
+typedef enum {
+    QG_OP_S8 = 0, QG_OP_S4 = 1, QG_OP_F16 = 2, QG_OP_W4A16 = 3, QG_OP_W4A4 = 4
+} qg_op;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qg_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int qg_version(void);
+
+/* Bytes of workspace the call `op` needs for an M x N x K problem (0 if none).
+ * For QG_OP_W4A4, K is the quantized reduction dimension (the size covers a
+ * low-rank term of rank up to 32). */
+size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: QG_OK, or QG_ERR_TIMEOUT if any kernel since the last
+ * call gave up on a bounded wait.  A failed CUDA call returns QG_ERR_CUDA. */
+int qg_device_status(void *stream);
+
+/* Sets the limit of every device-side wait, in nanoseconds (default 2e9;
+ * also read once from the environment variable QG_TIMEOUT_NS).  0 restores
+ * the default. */
+int qg_set_timeout_ns(uint64_t ns);
+
+/* Testing hook: K-chunk length of qgemm_s8, in blocks of 64 (1..16, default
+ * 16 = 1024).  Every chunk's fp32 partial sums stay within 2^24 for any
+ * value in 1..16; shorter chunks only cost more accumulator drains. */
+int qg_set_s8_chunk(int kblocks);
+
+/* [L4] Exact INT8 GEMM:  C[i][j] = sum_k A[i][k] * B[j][k]  (int32 result).
+ *  A : int8, M x K row-major, lda >= K.
+ *  B : int8, K-major (N x K row-major bytes), ldb >= K.
+ *  C : int32, M x N row-major, ldc >= N.
+ *  K : multiple of 16, K < 131072 (so every int32 result is exact).
+ *  ws: workspace of qg_workspace_size(QG_OP_S8, M, N, K) bytes, 256-byte
+ *      aligned, device memory; contents on entry are ignored.
+ * The result is bit-exact (integer arithmetic is exact). */
+int qgemm_s8(int64_t M, int64_t N, int64_t K,
+             const int8_t *A, int64_t lda, int layout_a,
+             const int8_t *B, int64_t ldb, int layout_b,
+             int32_t *C, int64_t ldc,
+             void *ws, size_t ws_bytes, void *stream);
+
+/* [L4] Exact INT4 GEMM on s4p operands:  C = A . B^T  (int32 result).
+ *  A : s4p, M x K values, lda_bytes >= K/2.
+ *  B : s4p, K-major (N x K values), ldb_bytes >= K/2.
+ *  C : int32, M x N row-major, ldc >= N.
+ *  K : multiple of 32, K < 262144.
+ *  ws: workspace of qg_workspace_size(QG_OP_S4, M, N, K) bytes, 256-byte aligned.
+ * The result is bit-exact. */
+int qgemm_s4(int64_t M, int64_t N, int64_t K,
+             const uint8_t *A, int64_t lda_bytes, int layout_a,
+             const uint8_t *B, int64_t ldb_bytes, int layout_b,
+             int32_t *C, int64_t ldc,
+             void *ws, size_t ws_bytes, void *stream);
+
+/* [L4] FP16 GEMM, fp32 accumulation, fp16 result rounded to nearest even:
+ *  C = A . B^T.  A: M x K row-major, B: K-major (N x K), C: M x N row-major.
+ *  K : multiple of 8.  No workspace. */
+int gemm_f16(int64_t M, int64_t N, int64_t K,
+             const uint16_t *A, int64_t lda, int layout_a,
+             const uint16_t *B, int64_t ldb, int layout_b,
+             uint16_t *C, int64_t ldc, void *stream);
+
+/* [SM75] W4A16 weight-only linear:
+ *  Y[m][n] = sum_k X[m][k] * (Wq[n][k] * Wscale[n][k / group]),
+ *  fp32 accumulation, fp16 result.
+ *  X      : fp16, M x K row-major, ldx >= K.
+ *  Wq     : s4p, N x K values, packed contiguously (N rows of K/2 bytes).
+ *  Wscale : fp16, N x (K/group), contiguous.  No zero points.
+ *  group  : 128 (the only group size this build supports).
+ *  Y      : fp16, M x N row-major, ldy >= N.
+ *  K      : multiple of `group`.  No workspace. */
+int w4a16_gemm(int64_t M, int64_t N, int64_t K,
+               const uint16_t *X, int64_t ldx,
+               const uint8_t *Wq, const uint16_t *Wscale, int64_t group,
+               uint16_t *Y, int64_t ldy, void *stream);
+
+/* [W4A4] Activation quantizer Q(X) with the fused low-rank down-projection:
+ *  per row m and K-block j (block elements):
+ *    s = fp16(max|x| / 7)           (binary32 division, round to nearest even)
+ *    q = s == 0 ? 0 : clamp(rint(x / s), -8, 7)   (binary32 division by the
+ *        rounded scale, rint round-half-even)
+ *  and XU = X . U rounded to fp16 (fp32 accumulation).
+ *  X      : fp32, M x K row-major, ldx >= K.
+ *  U      : fp16, K x rank row-major (may be NULL when rank == 0).
+ *  Xq     : s4p output, M x K values, contiguous (M rows of K/2 bytes).
+ *  Xscale : fp16 output, M x (K/block), contiguous.
+ *  XU     : fp16 output, M x rank, contiguous (ignored when rank == 0).
+ *  block  : 64 (the only block size this build supports); K multiple of block.
+ *  rank   : 0 or 32.
+ * The same call quantizes weights (rank 0).  Xq and Xscale are bit-exact
+ * with the definition above. */
+int w4a4_quantize(int64_t M, int64_t K, const float *X, int64_t ldx,
+                  const uint16_t *U, int64_t rank,
+                  uint8_t *Xq, uint16_t *Xscale, uint16_t *XU,
+                  int64_t block, void *stream);
+
+/* [W4A4] Y = (Q(X).Q(W)^T) (.) scale + L(X) + b, with the block-wise scale
+ * applied inside the K-sum:
+ *  Y[m][n] = sum_j Xscale[m][j]*Wscale[n][j] * sum_{k in block j} Xq[m][k]*Wq[n][k]
+ *          + sum_r XU[m][r] * V[r][n] + bias[n],
+ *  fp32 accumulation, fp16 result.
+ *  Xq, Xscale : as produced by w4a4_quantize (M rows).
+ *  Wq, Wscale : the same format for W (N rows).
+ *  XU : fp16 M x rank, V : fp16 rank x N row-major, rank 0 or 32 (XU and V
+ *       may be NULL when rank == 0).  bias : fp16 N, or NULL.
+ *  block : 64.  K multiple of 64.  Y : fp16 M x N row-major, ldy >= N.
+ *  ws : workspace of qg_workspace_size(QG_OP_W4A4, M, N, K) bytes, 256-byte
+ *       aligned. */
+int w4a4_gemm(int64_t M, int64_t N, int64_t K,
+              const uint8_t *Xq, const uint16_t *Xscale,
+              const uint8_t *Wq, const uint16_t *Wscale, int64_t block,
+              const uint16_t *XU, const uint16_t *V, int64_t rank,
+              const uint16_t *bias, uint16_t *Y, int64_t ldy,
+              void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMM_H */

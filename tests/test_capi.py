@@ -1,0 +1,71 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol,
+and rejects bad arguments synchronously (before touching any GPU)."""
+import pytest
+
+import bit_quantized_tensor_gb300 as qg
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return qg.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = qg.header_functions()
+    assert len(names) >= 12
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(names) == set(qg.SIGNATURES)
+
+
+def test_status_strings(L):
+    for code, name in qg.STATUS_NAMES.items():
+        assert L.qg_status_string(code).decode() == name
+    assert L.qg_status_string(99).decode() == "QG_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(L):
+    assert L.qg_workspace_size(qg.QG_OP_S8, 512, 512, 512) == 2 * 512 * 512 * 2
+    assert L.qg_workspace_size(qg.QG_OP_S4, 100, 50, 64) == 6400 + 3328
+    assert L.qg_workspace_size(qg.QG_OP_F16, 512, 512, 512) == 0
+    assert L.qg_workspace_size(qg.QG_OP_S8, 0, 5, 5) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+WS = 0x20000
+
+
+def _s8(L, M=64, N=64, K=64, A=FAKE, lda=64, la=0, B=FAKE, ldb=64, lb=1, C=FAKE, ldc=64,
+        ws=WS, wsb=1 << 30):
+    return L.qgemm_s8(M, N, K, A, lda, la, B, ldb, lb, C, ldc, ws, wsb, None)
+
+
+def test_qgemm_s8_argument_errors(L):
+    assert _s8(L, M=0) == 1
+    assert _s8(L, A=0) == 1
+    assert _s8(L, K=40) == 1                 # K % 16
+    assert _s8(L, lda=32) == 1               # lda < K
+    assert _s8(L, la=1) == 2                 # layout
+    assert _s8(L, lb=0) == 2
+    assert _s8(L, A=FAKE + 8) == 3           # misaligned pointer
+    assert _s8(L, lda=72) == 3               # lda not a multiple of 16 bytes
+    assert _s8(L, wsb=10) == 4               # workspace too small
+    assert _s8(L, ws=0) == 4
+    assert _s8(L, ws=WS + 16) == 3           # workspace not 256-byte aligned
+
+
+def test_gemm_f16_and_s4_argument_errors(L):
+    assert L.gemm_f16(64, 64, 12, FAKE, 64, 0, FAKE, 64, 1, FAKE, 64, None) == 1
+    assert L.gemm_f16(64, 64, 64, FAKE, 64, 0, FAKE, 64, 0, FAKE, 64, None) == 2
+    assert L.gemm_f16(64, 64, 64, FAKE, 68, 0, FAKE, 64, 1, FAKE, 64, None) == 3
+    assert L.qgemm_s4(64, 64, 48, FAKE, 32, 0, FAKE, 32, 1, FAKE, 64, WS, 1 << 30, None) == 1
+    assert L.qgemm_s4(64, 64, 64, FAKE, 40, 0, FAKE, 32, 1, FAKE, 64, WS, 1 << 30, None) == 3
+
+
+def test_no_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _s8(L) == 5
