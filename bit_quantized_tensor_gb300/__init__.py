@@ -53,6 +53,7 @@ SIGNATURES = {
     "qg_device_status": (_int, [_p]),
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
     "qg_set_s8_chunk": (_int, [_int]),
+    "qg_set_pdl": (_int, [_int]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "qgemm_s4": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "gemm_f16": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),

@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Returns false (after recording QG_ERR_TIMEOUT with the call-site tag) when
 // the limit runs out, or when another role of this CTA has already set
 // `*abort_flag`.  `abort_flag` may be null (drain waits ignore aborts).
-__device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           const Ctl& ctl, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();

@@ -1,5 +1,269 @@
-#include "qg_internal.h"
-extern "C" int w4a16_gemm(int64_t, int64_t, int64_t, const uint16_t*, int64_t, const uint8_t*,
-                          const uint16_t*, int64_t, uint16_t*, int64_t, void*) {
-    return QG_ERR_UNSUPPORTED;
+// W4A16 weight-only linear ("fused-int4-gemm-sm75" README: packed INT4
+// weights, sign extension and dequantization in registers, tensor-core MMA,
+// per-group scales with group_size = 128):
+//
+//   Y[m][n] = sum_k X[m][k] * (q[n][k] * s[n][k / 128]),  fp32 accumulation.
+//
+// Decode shapes (small M) are bound by streaming the packed weights from
+// HBM, so the kernel is organized around that stream:
+//  - every thread issues all of its weight loads (16 bytes per 128-wide
+//    group) at entry, before anything else, so each SM keeps tens of KB of
+//    weight reads in flight;
+//  - with programmatic dependent launch the weight and scale loads are issued
+//    before the previous kernel on the stream has finished; X (possibly that
+//    kernel's output) is read only after griddepcontrol.wait;
+//  - a 32-bit word of 8 nibbles is turned into four fp16 pairs with an XOR
+//    (two's complement -> offset binary), a mask-or into the fp16 pattern of
+//    1024 + n, and one fp16 subtraction of 1032: exact, ~1 instruction per
+//    value;
+//  - the dequantized pairs feed mma.sync m16n8k16 (fp16 x fp16 -> fp32) as
+//    the B operand; because a dot product does not depend on the order of k,
+//    each thread's logical MMA k slots are mapped onto the physical k of the
+//    word it loaded (pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7)), and the same
+//    mapping is applied to the X fragments, which are loaded 16 bytes at a
+//    time and regrouped with byte permutes;
+//  - each group's MMAs accumulate into a fresh fp32 tile that is scaled by
+//    the group's fp16 scales in fp32 and added to the running sum, so the
+//    weights are never rounded after dequantization;
+//  - the K range is split over the CTA's warps and the partial tiles are
+//    added through shared memory.
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "qg_ptx.cuh"
+
+namespace qg {
+
+constexpr int kGroup = 128;
+constexpr int kW16Threads = 256;   // 8 warps
+// Groups whose weights are in flight per thread: all 8 for decode shapes,
+// fewer when more m16 tiles need registers.
+template <int MT>
+__host__ __device__ constexpr int w16_batch() { return MT <= 1 ? 8 : (MT == 2 ? 4 : 2); }
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four fp16 pairs of the 8 signed nibbles of `w` (nibble j = physical k_j):
+// p[0] = (k0, k4), p[1] = (k1, k5), p[2] = (k2, k6), p[3] = (k3, k7).
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t u = w ^ 0x88888888u;  // nibble n -> n ^ 8 = value + 8 in [0, 15]
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t h = ((u >> (4 * j)) & 0x000F000Fu) | 0x64006400u;  // 1024 + (value + 8)
+        __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+        p[j] = *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// X fragment words for physical k = k0 .. k0+7 of one row, regrouped as the
+// pairs (x0,x4), (x1,x5), (x2,x6), (x3,x7).
+__device__ __forceinline__ void x_pairs(const __half* row, uint32_t (&p)[4]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row));
+    p[0] = __byte_perm(v.x, v.z, 0x5410);
+    p[1] = __byte_perm(v.x, v.z, 0x7632);
+    p[2] = __byte_perm(v.y, v.w, 0x5410);
+    p[3] = __byte_perm(v.y, v.w, 0x7632);
+}
+
+// MT: m16 tiles per CTA (M <= 16*MT); NT: n8 tiles per CTA; the CTA's 8
+// warps are NT n-tiles x (8/NT) K slices.
+template <int MT, int NT>
+__global__ void __launch_bounds__(kW16Threads)
+    k_w4a16(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
+            const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
+            int64_t ldy) {
+    constexpr int KQ = 8 / NT;
+    constexpr int kW16Batch = w16_batch<MT>();
+    __shared__ float red[8][MT * 4][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = warp % NT, kq = warp / NT;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup;
+    const int gpw = (G + KQ - 1) / KQ;
+    const int gbeg = min(G, kq * gpw), gend = min(G, gbeg + gpw);
+    const int n0 = (blockIdx.x * NT + nt) * 8;
+    const int wrow = n0 + g;          // W row whose bytes this lane loads
+    const int c0 = n0 + 2 * t;        // the two output columns this lane accumulates
+    const int64_t wstride = K / 2;
+    const int64_t sstride = G;
+
+    pdl_launch_dependents();
+
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+
+    bool waited = false;
+    for (int gb = gbeg; gb < gend; gb += kW16Batch) {
+        uint4 w[kW16Batch];
+        float s0[kW16Batch], s1[kW16Batch];
+#pragma unroll
+        for (int b = 0; b < kW16Batch; ++b) {
+            const int gi = gb + b;
+            w[b] = make_uint4(0u, 0u, 0u, 0u);  // decodes to zeros
+            s0[b] = 0.f;
+            s1[b] = 0.f;
+            if (gi < gend) {
+                if (wrow < N) w[b] = ld_stream_u4(Wq + wrow * wstride + gi * 64 + 16 * t);
+                if (c0 < N) s0[b] = __half2float(S[c0 * sstride + gi]);
+                if (c0 + 1 < N) s1[b] = __half2float(S[(c0 + 1) * sstride + gi]);
+            }
+        }
+        if (!waited) {
+            pdl_wait_prior_grid();  // X may be the previous kernel's output
+            waited = true;
+        }
+#pragma unroll
+        for (int b = 0; b < kW16Batch; ++b) {
+            const int gi = gb + b;
+            if (gi >= gend) break;
+            float tmp[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tmp[mt][i] = 0.f;
+            const uint32_t wv[4] = {w[b].x, w[b].y, w[b].z, w[b].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t p[4];
+                dequant_word(wv[i], p);
+                const int kx = gi * kGroup + 32 * t + 8 * i;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int ra = mt * 16 + g, rb = ra + 8;
+                    uint32_t xa[4] = {0u, 0u, 0u, 0u}, xb[4] = {0u, 0u, 0u, 0u};
+                    if (ra < M) x_pairs(X + ra * ldx + kx, xa);
+                    if (rb < M) x_pairs(X + rb * ldx + kx, xb);
+                    const uint32_t a0[4] = {xa[0], xb[0], xa[1], xb[1]};
+                    const uint32_t a1[4] = {xa[2], xb[2], xa[3], xb[3]};
+                    mma_16816(tmp[mt], a0, p[0], p[1]);
+                    mma_16816(tmp[mt], a1, p[2], p[3]);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] = fmaf(tmp[mt][0], s0[b], acc[mt][0]);
+                acc[mt][1] = fmaf(tmp[mt][1], s1[b], acc[mt][1]);
+                acc[mt][2] = fmaf(tmp[mt][2], s0[b], acc[mt][2]);
+                acc[mt][3] = fmaf(tmp[mt][3], s1[b], acc[mt][3]);
+            }
+        }
+    }
+    if (!waited) pdl_wait_prior_grid();
+
+    // Sum the KQ partial tiles of each n tile.
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[warp][mt * 4 + i][lane] = acc[mt][i];
+    __syncthreads();
+    if (kq != 0) return;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < KQ; ++q) sum += red[q * NT + nt][mt * 4 + i][lane];
+            v[i] = sum;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = mt * 16 + g + 8 * h;
+            if (row >= M) continue;
+            __half* dst = Y + row * ldy + c0;
+            if (c0 + 1 < N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(v[2 * h], v[2 * h + 1]);
+            } else {
+                if (c0 < N) dst[0] = __float2half_rn(v[2 * h]);
+                if (c0 + 1 < N) dst[1] = __float2half_rn(v[2 * h + 1]);
+            }
+        }
+    }
+}
+
+static std::atomic<int> g_w4a16_pdl{1};
+
+template <int MT, int NT>
+static int launch_w4a16(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
+                        const __half* S, __half* Y, int64_t ldy, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + 8 * NT - 1) / (8 * NT)));
+    cfg.blockDim = dim3(kW16Threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16<MT, NT>, M, N, K, X, ldx, Wq, S, Y, ldy));
+}
+
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+int qg_set_pdl(int enable) {
+    g_w4a16_pdl.store(enable ? 1 : 0);
+    return QG_OK;
+}
+
+int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, const uint8_t* Wq,
+               const uint16_t* Wscale, int64_t group, uint16_t* Y, int64_t ldy, void* stream) {
+    if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return QG_ERR_INVALID_ARG;
+    if (group != kGroup) return QG_ERR_UNSUPPORTED;
+    if (K % kGroup) return QG_ERR_INVALID_ARG;
+    if (!X || !Wq || !Wscale || !Y) return QG_ERR_INVALID_ARG;
+    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wscale) || !aligned16(Y) || ldx % 8)
+        return QG_ERR_MISALIGNED;
+    if (current_device() < 0) return QG_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const __half* Xh = reinterpret_cast<const __half*>(X);
+    const __half* Sh = reinterpret_cast<const __half*>(Wscale);
+    __half* Yh = reinterpret_cast<__half*>(Y);
+    const int n = static_cast<int>(N), k = static_cast<int>(K);
+    // Rows are processed in chunks of up to 128 (8 m16 tiles per CTA).
+    for (int64_t r0 = 0; r0 < M; r0 += 128) {
+        const int m = static_cast<int>(M - r0 < 128 ? M - r0 : 128);
+        const __half* Xr = Xh + r0 * ldx;
+        __half* Yr = Yh + r0 * ldy;
+        int rc;
+        if (m <= 16)
+            rc = launch_w4a16<1, 2>(m, n, k, Xr, ldx, Wq, Sh, Yr, ldy, s);
+        else if (m <= 32)
+            rc = launch_w4a16<2, 4>(m, n, k, Xr, ldx, Wq, Sh, Yr, ldy, s);
+        else if (m <= 64)
+            rc = launch_w4a16<4, 8>(m, n, k, Xr, ldx, Wq, Sh, Yr, ldy, s);
+        else
+            rc = launch_w4a16<8, 8>(m, n, k, Xr, ldx, Wq, Sh, Yr, ldy, s);
+        if (rc) return rc;
+    }
+    return QG_OK;
+}
+
+}  // extern "C"

@@ -89,6 +89,14 @@ int qg_set_timeout_ns(uint64_t ns);
  * value in 1..16; shorter chunks only cost more accumulator drains. */
 int qg_set_s8_chunk(int kblocks);
 
+/* Programmatic dependent launch of w4a16_gemm (default on).  When on, a
+ * w4a16_gemm kernel may start while the previous kernel on the stream is
+ * still running: it streams Wq and Wscale at once and reads X only after
+ * that kernel has completed.  Wq and Wscale must therefore not be written by
+ * the kernel launched just before it on the same stream; pass 0 to turn the
+ * overlap off. */
+int qg_set_pdl(int enable);
+
 /* [L4] Exact INT8 GEMM:  C[i][j] = sum_k A[i][k] * B[j][k]  (int32 result).
  *  A : int8, M x K row-major, lda >= K.
  *  B : int8, K-major (N x K row-major bytes), ldb >= K.

@@ -69,3 +69,28 @@ def test_no_gpu_reports_cuda_error(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _s8(L) == 5
+
+
+def test_w4a16_and_w4a4_argument_errors(L):
+    # w4a16_gemm(M, N, K, X, ldx, Wq, Wscale, group, Y, ldy, stream)
+    assert L.w4a16_gemm(1, 64, 100, FAKE, 128, FAKE, FAKE, 128, FAKE, 64, None) == 1  # K % group
+    assert L.w4a16_gemm(1, 64, 128, FAKE, 128, FAKE, FAKE, 64, FAKE, 64, None) == 2   # group
+    assert L.w4a16_gemm(1, 64, 128, FAKE, 100, FAKE, FAKE, 128, FAKE, 64, None) == 1  # ldx < K
+    assert L.w4a16_gemm(1, 64, 128, FAKE, 132, FAKE, FAKE, 128, FAKE, 64, None) == 3  # ldx % 8
+    assert L.w4a16_gemm(1, 64, 128, FAKE + 2, 128, FAKE, FAKE, 128, FAKE, 64, None) == 3
+    # w4a4_quantize(M, K, X, ldx, U, rank, Xq, Xs, XU, block, stream)
+    assert L.w4a4_quantize(4, 96, FAKE, 96, None, 0, FAKE, FAKE, None, 64, None) == 1  # K % 64
+    assert L.w4a4_quantize(4, 128, FAKE, 128, None, 0, FAKE, FAKE, None, 32, None) == 2
+    assert L.w4a4_quantize(4, 128, FAKE, 128, FAKE, 16, FAKE, FAKE, FAKE, 64, None) == 2
+    assert L.w4a4_quantize(4, 128, FAKE, 128, None, 32, FAKE, FAKE, FAKE, 64, None) == 1
+    assert L.w4a4_quantize(4, 128, FAKE, 130, None, 0, FAKE, FAKE, None, 64, None) == 3
+    # w4a4_gemm(M, N, K, Xq, Xs, Wq, Ws, block, XU, V, rank, bias, Y, ldy, ws, wsb, stream)
+    big = 1 << 30
+    assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 32, None, None, 0, None, FAKE, 8,
+                       WS, big, None) == 2
+    assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 32, None, FAKE, 8,
+                       WS, big, None) == 1
+    assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, None, FAKE, 8,
+                       WS, 16, None) == 4
+    assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, None, FAKE, 4,
+                       WS, big, None) == 1
