@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized tensor-core GEMM path on GB300.
+
+One step = one pass of the whole hot path over synthetic inputs resident in
+HBM:
+  qgemm_s8   8192 x 8192 x 8192, int8 uniform [-128,127]  -> int32 (exact)
+  qgemm_s4   8192 x 8192 x 8192, int4 uniform [-8,7]      -> int32 (exact)
+  gemm_f16   8192 x 8192 x 8192, N(0,1) fp16 -> fp16 (fp32 accumulation)
+  w4a16_gemm M=1, N=K=4096, group 128, one call per weight set over a
+             rotation of distinct weight sets totalling > 2x L2 (a decode
+             step through consecutive layers)
+  w4a4       quantize X (4096 x 8192 fp32) with X.U (rank 32), then the
+             block-scaled GEMM against pre-quantized W (8192 x 8192) + XU.V + b
+L2 is flushed (a 256 MiB write) before every op; every op's working set is
+also larger than L2.
+
+Headline `value`: INT8 GEMM TOPS at N=8192 (2*N^3 / time of qgemm_s8,
+including its operand conversion).  `breakdown` holds every op's throughput
+and roofline fraction.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT8/INT4 GEMM TOPS at N=8192 & % tensor peak; W4A16 M=1 HBM GB/s"
+N_SQ = 8192
+W16_N = W16_K = 4096
+W4_M, W4_N, W4_K, W4_R = 4096, 8192, 8192, 32
+FLUSH_BYTES = 256 << 20
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense tensor rates relative to bf16/fp16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
+FP8_RATIO, FP4_RATIO = 2.0, 6.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload
+
+class Workload:
+    """Synthetic inputs of every op, resident on the device."""
+
+    def __init__(self, dev):
+        import numpy as np
+        import torch
+        import bit_quantized_tensor_gb300 as qg
+        from bit_quantized_tensor_gb300 import inputs
+        self.qg, self.torch, self.dev = qg, torch, dev
+
+        def t(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        n = N_SQ
+        self.A8, self.B8 = t(inputs.s8_uniform(n, n, 1002)), t(inputs.s8_uniform(n, n, 2002))
+        self.A4 = t(inputs.s4_packed_uniform(n, n, 1002))
+        self.B4 = t(inputs.s4_packed_uniform(n, n, 2002))
+        self.Af, self.Bf = t(inputs.f16_normal(n, n, 1002)), t(inputs.f16_normal(n, n, 2002))
+        self.C32 = torch.empty((n, n), dtype=torch.int32, device=dev)
+        self.C16 = torch.empty((n, n), dtype=torch.float16, device=dev)
+        self.ws8 = torch.empty(qg.workspace_size(qg.QG_OP_S8, n, n, n), dtype=torch.uint8, device=dev)
+        self.ws4 = torch.empty(qg.workspace_size(qg.QG_OP_S4, n, n, n), dtype=torch.uint8, device=dev)
+
+        # W4A16: distinct weight sets totalling more than 2x L2
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        per_set = W16_N * W16_K // 2 + W16_N * (W16_K // 128) * 2
+        self.w16_sets = max(8, 2 * l2 // per_set + 2)
+        self.X16 = t(inputs.f16_normal(1, W16_K, 1003))
+        self.W16 = [t(inputs.s4_packed_uniform(W16_N, W16_K, 2003 + 100 * i))
+                    for i in range(self.w16_sets)]
+        self.S16 = [t(inputs.f16_uniform(W16_N, W16_K // 128, 0.005, 0.02, 3003 + 100 * i))
+                    for i in range(self.w16_sets)]
+        self.Y16 = torch.empty((1, W16_N), dtype=torch.float16, device=dev)
+        self.w16_bytes = per_set + 2 * W16_K + 2 * W16_N
+
+        # W4A4: weights quantized once (outside any timed region)
+        self.X4 = t(inputs.f32_normal(W4_M, W4_K, 1004))
+        Wf = t(inputs.f32_normal(W4_N, W4_K, 2004))
+        self.U = t(inputs.f16_normal(W4_K, W4_R, 3004, sigma=0.02))
+        self.V = t(inputs.f16_normal(W4_R, W4_N, 3005, sigma=0.02))
+        self.bias = t(inputs.f16_normal(1, W4_N, 3006, sigma=0.1)[0])
+        self.qw, self.sw, _ = qg.w4a4_quantize(Wf)
+        del Wf
+        self.q_out = (torch.empty((W4_M, W4_K // 2), dtype=torch.uint8, device=dev),
+                      torch.empty((W4_M, W4_K // 64), dtype=torch.float16, device=dev),
+                      torch.empty((W4_M, W4_R), dtype=torch.float16, device=dev))
+        self.Y4 = torch.empty((W4_M, W4_N), dtype=torch.float16, device=dev)
+        self.ws_w4 = torch.empty(qg.workspace_size(qg.QG_OP_W4A4, W4_M, W4_N, W4_K),
+                                 dtype=torch.uint8, device=dev)
+        self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        # The decode rotation is replayed as one CUDA graph (programmatic
+        # dependent launch edges are kept), so host launch cost is not timed.
+        self._w4a16_calls()
+        torch.cuda.synchronize()
+        self.w16_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.w16_graph):
+            self._w4a16_calls()
+        torch.cuda.synchronize()
+
+    # each op returns the number of library kernels it launched
+    def s8(self):
+        self.qg.qgemm_s8(self.A8, self.B8, C=self.C32, ws=self.ws8)
+        return 3
+
+    def s4(self):
+        self.qg.qgemm_s4(self.A4, self.B4, N_SQ, C=self.C32, ws=self.ws4)
+        return 3
+
+    def f16(self):
+        self.qg.gemm_f16(self.Af, self.Bf, C=self.C16)
+        return 1
+
+    def _w4a16_calls(self):
+        for i in range(self.w16_sets):
+            self.qg.w4a16_gemm(self.X16, self.W16[i], self.S16[i], Y=self.Y16)
+
+    def w4a16(self):
+        self.w16_graph.replay()
+        return self.w16_sets
+
+    def w4a4_quant(self):
+        self.qg.w4a4_quantize(self.X4, self.U, out=self.q_out)
+        return 1
+
+    def w4a4_gemm(self):
+        q, s, xu = self.q_out
+        self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, V=self.V, bias=self.bias,
+                          Y=self.Y4, ws=self.ws_w4)
+        return 4
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+
+OPS = ["s8", "s4", "f16", "w4a16", "w4a4_quant", "w4a4_gemm"]
+MAIN_KERNEL_OPS = {"s8", "s4", "f16", "w4a4_gemm"}  # ops with a timed tcgen05 GEMM kernel
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import bit_quantized_tensor_gb300 as qg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    qg.lib()
+    wl = Workload(dev)
+    stream = torch.cuda.current_stream()
+
+    ev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for op in OPS}
+    kev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] for op in MAIN_KERNEL_OPS}
+    for lst in list(ev.values()) + list(kev.values()):
+        for a, b in lst:  # instantiate the driver events
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        launches = 0
+        for op in OPS:
+            wl.flush()
+            if i is not None and op in kev:
+                k0, k1 = kev[op][i]
+                qg.lib().qg_set_profile_events(k0.cuda_event, k1.cuda_event)
+            if i is not None:
+                ev[op][i][0].record(stream)
+            launches += getattr(wl, op)()
+            if i is not None:
+                ev[op][i][1].record(stream)
+            qg.lib().qg_set_profile_events(None, None)
+        return launches
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    assert qg.device_status() == qg.QG_OK, "device-side wait timed out during warm-up"
+
+    clocks = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    launches = 0
+    for i in range(args.steps):
+        launches += step(i)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    assert qg.device_status() == qg.QG_OK, "device-side wait timed out in the timed region"
+
+    t_op = {op: [a.elapsed_time(b) for a, b in ev[op]] for op in OPS}          # ms
+    t_k = {op: [a.elapsed_time(b) for a, b in kev[op]] for op in MAIN_KERNEL_OPS}
+    step_ms = [sum(t_op[op][i] for op in OPS) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    peaks, peak_src = load_peaks()
+    bf16 = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    med = {op: statistics.median(v) for op, v in t_op.items()}
+    medk = {op: statistics.median(v) for op, v in t_k.items()}
+    gemm_ops = 2.0 * N_SQ ** 3
+    w4_ops = 2.0 * W4_M * W4_N * W4_K + 2.0 * W4_M * W4_N * W4_R
+
+    def tops(ops, ms):
+        return ops / (ms * 1e-3) / 1e12
+
+    s8_tops = sum(gemm_ops for _ in t_op["s8"]) / (sum(t_op["s8"]) * 1e-3) / 1e12
+    if dist and world > 1:
+        tt = torch.tensor([sum(t_op["s8"])], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        s8_tops = world * gemm_ops * args.steps / (float(tt.item()) * 1e-3) / 1e12
+
+    w16_call_us = med["w4a16"] * 1e3 / wl.w16_sets
+    w16_gbs = wl.w16_bytes / (w16_call_us * 1e-6) / 1e9
+    breakdown = {
+        "int8_gemm_8192": {"TOPS": round(tops(gemm_ops, med["s8"]), 1),
+                           "kernel_TOPS": round(tops(gemm_ops, medk["s8"]), 1),
+                           "mma_kind": "f16 (int8 carried exactly in fp16, fp32 chunks of K<=1024)",
+                           "frac_of_f16_peak": round(tops(gemm_ops, med["s8"]) / bf16, 3)},
+        "int4_gemm_8192": {"TOPS": round(tops(gemm_ops, med["s4"]), 1),
+                           "kernel_TOPS": round(tops(gemm_ops, medk["s4"]), 1),
+                           "mma_kind": "f8f6f4 e4m3 (int4 carried exactly)",
+                           "frac_of_fp8_peak": round(tops(gemm_ops, med["s4"]) / (FP8_RATIO * bf16), 3)},
+        "fp16_gemm_8192": {"TFLOPS": round(tops(gemm_ops, med["f16"]), 1),
+                           "frac_of_f16_peak": round(tops(gemm_ops, med["f16"]) / bf16, 3)},
+        "w4a16_m1_4096": {"GB/s": round(w16_gbs, 1), "us_per_call": round(w16_call_us, 3),
+                          "frac_of_hbm": round(w16_gbs / hbm, 3), "weight_sets": wl.w16_sets,
+                          "launch": "CUDA graph of the rotation, programmatic dependent launch"},
+        "w4a4_4096x8192x8192_r32": {
+            "quantize_us": round(med["w4a4_quant"] * 1e3, 1),
+            "quantize_GB/s": round(W4_M * W4_K * 4 / (med["w4a4_quant"] * 1e-3) / 1e9, 1),
+            "gemm_us": round(med["w4a4_gemm"] * 1e3, 1),
+            "TOPS": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]), 1),
+            "kernel_TOPS": round(tops(w4_ops, medk["w4a4_gemm"]), 1),
+            "mma_kind": "f16 (block scales folded into fp16 operands)",
+            "frac_of_f16_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]) / bf16, 3),
+            "mfu_vs_fp4_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"])
+                                     / (FP4_RATIO * bf16), 3)},
+        "op_ms_median": {op: round(v, 4) for op, v in med.items()},
+    }
+    k_ms = medk["s8"]
+    achieved = tops(gemm_ops, k_ms)
+    roofline = {"bound": "tensor", "kernel": "tc_gemm_kernel<F16,S32> (qgemm_s8 main GEMM)",
+                "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 dense (fp16 kind runs at the bf16 rate)",
+                "frac": round(achieved / bf16, 3), "traffic": None}
+
+    result = {
+        "metric": METRIC, "value": round(s8_tops, 1), "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": "INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1 N=K=4096 g128, "
+                               "W4A4 4096x8192x8192 r32 (one step = all six ops)",
+                   "N": N_SQ, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "256 MiB write before every op; every working set > L2",
+                   "wall_s_timed_region": round(wall, 3)},
+        "breakdown": breakdown, "roofline": roofline, "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and args.e2e:
+        result["e2e"] = measure_e2e(wl, args)
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        result["cpu_baseline"] = oracle_baseline(args.cpu_seconds)
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def measure_e2e(wl, args):
+    """qgemm_s8 through the public binding with host buffers: pinned H2D of A
+    and B, the GEMM, D2H of C, all inside the timed region."""
+    import torch
+    n = N_SQ
+    hA = wl.A8.cpu().pin_memory()
+    hB = wl.B8.cpu().pin_memory()
+    hC = torch.empty((n, n), dtype=torch.int32).pin_memory()
+    dA, dB = torch.empty_like(wl.A8), torch.empty_like(wl.B8)
+
+    def once():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        wl.qg.qgemm_s8(dA, dB, C=wl.C32, ws=wl.ws8)
+        hC.copy_(wl.C32, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        once()
+    ts = []
+    for _ in range(max(3, args.steps)):
+        t0 = time.perf_counter()
+        once()
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return {"value": round(2.0 * n ** 3 / t / 1e12, 1), "unit": "TOPS",
+            "h2d_bytes_per_step": 2 * n * n, "d2h_bytes_per_step": 4 * n * n,
+            "op": "qgemm_s8 8192^3 with pinned host buffers"}
+
+
+def oracle_baseline(seconds: float, rows: int | None = None):
+    """The CPU oracle on a bounded sample of the INT8 GEMM: `rows` rows of
+    C = A . B^T at N = K = 8192, timed on the host cores."""
+    import oracle
+    from bit_quantized_tensor_gb300 import inputs
+    oracle.build()
+    n = N_SQ
+    A = inputs.s8_uniform(n, n, 1002)
+    B = inputs.s8_uniform(n, n, 2002)
+    cores = oracle.threads()
+    if rows is None:
+        probe = max(cores, 4)
+        t0 = time.perf_counter()
+        oracle.gemm_s8(A[:probe], B)
+        dt = time.perf_counter() - t0
+        rows = int(min(n, max(probe, probe * seconds / max(dt, 1e-3))))
+        rows = max(cores, rows // cores * cores)
+    t0 = time.perf_counter()
+    oracle.gemm_s8(A[:rows], B)
+    dt = time.perf_counter() - t0
+    return {"value": round(2.0 * rows * n * n / dt / 1e12, 6), "unit": "TOPS", "cores": cores,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows} rows of the 8192^3 INT8 GEMM (C[rows] = A[rows] . B^T, int64 "
+                      f"accumulation), {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on the same metric."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    for _ in range(max(args.warmup, 0)):
+        oracle_baseline(0.5)
+    vals, t0 = [], time.perf_counter()
+    last = None
+    for _ in range(args.steps):
+        last = oracle_baseline(args.cpu_seconds / max(args.steps, 1))
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(wall * 1e3 / max(args.steps, 1), 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+           "config": {"workload": "INT8 GEMM 8192^3, bounded row sample per step (CPU oracle)",
+                      "N": N_SQ},
+           "cpu_baseline": {"value": value, "unit": "TOPS", "cores": last["cores"],
+                            "kind": "oracle", "sample": last["sample"]},
+           "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU seconds of the oracle baseline sample")
+    args = ap.parse_args()
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        import __graft_entry__
+        __graft_entry__.build_library()
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()
