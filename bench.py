@@ -328,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
             "gemm_us": round(med["w4a4_gemm"] * 1e3, 1),
             "TOPS": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]), 1),
             "kernel_TOPS": round(tops(w4_ops, medk["w4a4_gemm"]), 1),
-            "mma_kind": "f16 (block scales folded into fp16 operands)",
+            "mma_kind": "f8f6f4 e4m3 exact 64-block partials, scales applied in fp32",
             "frac_of_f16_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]) / bf16, 3),
             "mfu_vs_fp4_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"])
                                      / (FP4_RATIO * bf16), 3)},

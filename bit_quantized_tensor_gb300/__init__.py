@@ -51,9 +51,11 @@ SIGNATURES = {
     "qg_version": (_int, []),
     "qg_workspace_size": (_sz, [_int, _i64, _i64, _i64]),
     "qg_device_status": (_int, [_p]),
+    "qg_last_cuda_error": (_int, []),
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
+    "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "qgemm_s4": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "gemm_f16": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),
@@ -103,7 +105,11 @@ def _stream(stream=None) -> int:
 
 def _check(name: str, code: int) -> None:
     if code != QG_OK:
-        raise QgError(name, code)
+        err = QgError(name, code)
+        if code == 5:  # QG_ERR_CUDA: attach the failing CUDA call's code
+            err.cuda_error = int(lib().qg_last_cuda_error())
+            err.args = (f"{err.args[0]} (CUDA error code {err.cuda_error})",)
+        raise err
 
 
 def _cuda(t, dtype, name):

@@ -17,6 +17,7 @@ int* g_status_ptr[kMaxDevices] = {};
 std::once_flag g_status_once[kMaxDevices];
 int g_sms[kMaxDevices] = {};
 std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<int> g_last_cuda_error{0};
 
 uint64_t timeout_from_env() {
     const char* e = std::getenv("QG_TIMEOUT_NS");
@@ -30,6 +31,11 @@ uint64_t timeout_from_env() {
 }  // namespace
 
 namespace qg {
+
+int record_cuda_error(int code) {
+    g_last_cuda_error.store(code);
+    return QG_ERR_CUDA;
+}
 
 int current_device() {
     int d = 0;
@@ -98,14 +104,18 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
             return round_up256(2 * m * k) + round_up256(2 * n * k);
         case QG_OP_S4:  // e4m3 copies of both operands (exact for int4 values)
             return round_up256(m * k) + round_up256(n * k);
-        case QG_OP_W4A4: {  // fp16 scale-folded operands + up to 32 low-rank columns
-            const size_t ke = k + 32;
-            return round_up256(2 * m * ke) + round_up256(2 * n * ke);
+        case QG_OP_W4A4: {  // e4m3 operands, transposed fp32 scale tables, V^T
+            const size_t nblk = k / 64 + 1;
+            const size_t mp = (m + 3) & ~static_cast<size_t>(3), np = (n + 3) & ~static_cast<size_t>(3);
+            return round_up256(m * k) + round_up256(n * k) + round_up256(4 * nblk * mp) +
+                   round_up256(4 * nblk * np) + round_up256(2 * n * 32);
         }
         default:
             return 0;
     }
 }
+
+int qg_last_cuda_error(void) { return g_last_cuda_error.exchange(0); }
 
 int qg_set_timeout_ns(uint64_t ns) {
     g_timeout_ns.store(ns == 0 ? timeout_from_env() : ns);

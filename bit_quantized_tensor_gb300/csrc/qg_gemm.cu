@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qg_gemm_host.h"
@@ -42,22 +43,38 @@ static EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-int make_tmap_kmajor(CUtensorMap* map, bool fp16, const void* base, int64_t k_elems, int64_t rows,
-                     int64_t row_stride_bytes, int box_k, int box_rows) {
+int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int64_t inner,
+                 int64_t outer, int64_t row_stride_bytes, int box_inner, int box_outer,
+                 CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return QG_ERR_CUDA;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_elems), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? QG_OK : QG_ERR_CUDA;
+    return r == CUDA_SUCCESS ? QG_OK : record_cuda_error(-static_cast<int>(r));
+}
+
+int make_tmap_kmajor(CUtensorMap* map, bool fp16, const void* base, int64_t k_elems, int64_t rows,
+                     int64_t row_stride_bytes, int box_k, int box_rows) {
+    return make_tmap_2d(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        base, k_elems, rows, row_stride_bytes, box_k, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // ------------------------------------------------------------ tc GEMM launch
+
+// Caller-owned CUDA events recorded around every tcgen05 GEMM launch while
+// set (measurement of the main kernel alone); null = off.
+static std::atomic<void*> g_prof_before{nullptr}, g_prof_after{nullptr};
+
+void profile_events(void** before, void** after) {
+    *before = g_prof_before.load();
+    *after = g_prof_after.load();
+}
 
 template <class Cfg>
 static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ldb_bytes, int64_t M,
@@ -80,7 +97,7 @@ static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ld
             cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Cfg>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  Cfg::SMEM_BYTES);
-            if (e != cudaSuccess) return QG_ERR_CUDA;
+            if (e != cudaSuccess) return map_cuda(e);
             attr_set[dev] = true;
         }
     }
@@ -97,8 +114,13 @@ static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ld
     p.ctl = ctl;
     const int64_t tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
     const int grid = static_cast<int>(tiles < num_sms(dev) ? tiles : num_sms(dev));
+    cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_prof_before.load());
+    cudaEvent_t ev1 = static_cast<cudaEvent_t>(g_prof_after.load());
+    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return QG_ERR_CUDA;
     tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
-    return map_cuda(cudaGetLastError());
+    rc = map_cuda(cudaGetLastError());
+    if (!rc && ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return QG_ERR_CUDA;
+    return rc;
 }
 
 int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, int64_t M, int64_t N,
@@ -178,6 +200,12 @@ __global__ void k_s4_to_e4m3(const uint8_t* __restrict__ src, int64_t rows, int6
     }
 }
 
+int s4_to_e4m3(const uint8_t* src, int64_t rows, int64_t K, int64_t lds_bytes, uint8_t* dst,
+               int64_t ldd, int dev, cudaStream_t s) {
+    k_s4_to_e4m3<<<conv_grid(dev, rows * K / 32), 256, 0, s>>>(src, rows, K / 2, lds_bytes, dst, ldd);
+    return map_cuda(cudaGetLastError());
+}
+
 int conv_grid(int dev, int64_t work_items) {
     const int64_t per_block = 256;
     int64_t g = (work_items + per_block - 1) / per_block;
@@ -198,6 +226,13 @@ using namespace qg;
 static bool bad_layouts(int la, int lb) { return la != QG_ROW_MAJOR || lb != QG_COL_MAJOR; }
 
 extern "C" {
+
+int qg_set_profile_events(void* before, void* after) {
+    if ((before == nullptr) != (after == nullptr)) return QG_ERR_INVALID_ARG;
+    g_prof_before.store(before);
+    g_prof_after.store(after);
+    return QG_OK;
+}
 
 int qg_set_s8_chunk(int kblocks) {
     if (kblocks < 1 || kblocks > 16) return QG_ERR_INVALID_ARG;

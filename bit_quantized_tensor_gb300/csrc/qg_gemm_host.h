@@ -7,6 +7,15 @@
 
 namespace qg {
 
+// Encodes a 2-D tiled TMA map: `outer` rows of `inner` elements, rows
+// `row_stride_bytes` apart, box of box_inner x box_outer elements.
+int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int64_t inner,
+                 int64_t outer, int64_t row_stride_bytes, int box_inner, int box_outer,
+                 CUtensorMapSwizzle swizzle);
+
+// The caller-owned events of qg_set_profile_events (null when unset).
+void profile_events(void** before, void** after);
+
 // Encodes a 2-D TMA map over a K-major matrix (rows x k_elems, row stride in
 // bytes) with the 128-byte swizzle and a box of box_k x box_rows elements.
 // fp16 selects 2-byte elements, otherwise 1-byte elements.
@@ -21,5 +30,10 @@ int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, 
 
 // Grid size for the elementwise grid-stride kernels (256 threads per block).
 int conv_grid(int dev, int64_t work_items);
+
+// Packed signed 4-bit rows (K values, low nibble = even k) -> one e4m3 byte
+// per value (exact), enqueued on `s`.  K is a multiple of 32.
+int s4_to_e4m3(const uint8_t* src, int64_t rows, int64_t K, int64_t lds_bytes, uint8_t* dst,
+               int64_t ldd, int dev, cudaStream_t s);
 
 }  // namespace qg

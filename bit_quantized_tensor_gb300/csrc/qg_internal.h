@@ -40,6 +40,12 @@ int current_device();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-inline int map_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+// Records the code of a failed runtime call (positive) or driver call
+// (negative) for qg_last_cuda_error(); returns QG_ERR_CUDA.
+int record_cuda_error(int code);
+
+inline int map_cuda(cudaError_t e) {
+    return e == cudaSuccess ? QG_OK : record_cuda_error(static_cast<int>(e));
+}
 
 }  // namespace qg

@@ -5,15 +5,19 @@
 // w4a4_quantize  one pass over X (fp32): per row and 64-element K block the
 //                symmetric absmax quantizer (bit-exact IEEE binary32 steps),
 //                fused with the low-rank down-projection XU = X . U.
-// w4a4_gemm      folds each block scale into its 4-bit values (fp16 q*s, one
-//                rounding), appends the low-rank factors as `rank` extra K
-//                columns ([q*sX | XU] against [q*sW | V^T]), and runs the
-//                tcgen05 fp16 GEMM whose epilogue adds the bias per column.
-//                The block-wise scale therefore acts inside the K sum, block
-//                by block, as the scaled product requires.
+// w4a4_gemm      the block-scaled GEMM of w4a4_gemm.cuh: exact integer block
+//                partials on the tensor cores, both block scales applied in
+//                fp32 by the epilogue, the low-rank term as one extra MMA
+//                unit, the bias before the fp16 store.  A short pre-pass
+//                turns the packed operands into e4m3 bytes and the scales
+//                into transposed fp32 tables (one row per K block plus a
+//                constant-1 row for the low-rank unit).
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "qg_gemm_host.h"
+#include "w4a4_gemm.cuh"
 
 namespace qg {
 
@@ -160,57 +164,31 @@ __global__ void __launch_bounds__(kQThreads)
     }
 }
 
-// ------------------------------------------------ scale folding
-//
-// Dst[row][k] = fp16(q[row][k] * s[row][k / 64]) for k < K: the integer
-// times the fp16 scale is exact in fp32 and rounds once to fp16.  16 values
-// per thread (8 packed bytes, inside one block).
-__global__ void k_w4a4_fold(int64_t rows, int K, const uint8_t* __restrict__ Q,
-                            const __half* __restrict__ S, __half* __restrict__ Dst, int64_t ldd) {
-    const int per_row = K / 16;
-    const int64_t total = rows * per_row;
+// ------------------------------------------------ GEMM pre-pass
+
+// St[j][r] = S[r][j] (fp16 -> fp32) for j < nblk; St[nblk][r] = 1; columns
+// r in [rows, rows_p) are 0.  S: rows x nblk, St: (nblk + 1) x rows_p.
+__global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
+                                    const __half* __restrict__ S, float* __restrict__ St) {
+    const int64_t total = static_cast<int64_t>(nblk + 1) * rows_p;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / per_row;
-        const int c = static_cast<int>(i - r * per_row) * 16;
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(Q + r * (K / 2) + c / 2));
-        const float s = __half2float(S[r * (K / kW4A4Block) + c / kW4A4Block]);
-        uint32_t out[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t word = j < 4 ? w.x : w.y;
-            const int sh = 8 * (j & 3);
-            const int lo = static_cast<int>((word >> sh) & 0xFu);
-            const int hi = static_cast<int>((word >> (sh + 4)) & 0xFu);
-            const float vlo = static_cast<float>(lo < 8 ? lo : lo - 16) * s;
-            const float vhi = static_cast<float>(hi < 8 ? hi : hi - 16) * s;
-            __half2 h = __floats2half2_rn(vlo, vhi);
-            out[j] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        uint4* d = reinterpret_cast<uint4*>(Dst + r * ldd + c);
-        d[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        const int64_t j = i / rows_p;
+        const int64_t r = i - j * rows_p;
+        float v = 0.f;
+        if (r < rows) v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
+        St[i] = v;
     }
 }
 
-// Low-rank columns: A'[m][K + j] = XU[m][j] and B'[n][K + j] = V[j][n].
-__global__ void k_w4a4_lowrank_cols(int M, int N, int K, int rank, const __half* __restrict__ XU,
-                                    const __half* __restrict__ V, __half* __restrict__ A,
-                                    __half* __restrict__ B, int64_t ld) {
-    const int64_t totalA = static_cast<int64_t>(M) * rank;
-    const int64_t total = totalA + static_cast<int64_t>(N) * rank;
+// Vt[n][j] = V[j][n];  V: rank x N, Vt: N x rank.
+__global__ void k_transpose_v(int N, int rank, const __half* __restrict__ V, __half* __restrict__ Vt) {
+    const int64_t total = static_cast<int64_t>(N) * rank;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        if (i < totalA) {
-            const int64_t m = i / rank;
-            const int j = static_cast<int>(i - m * rank);
-            A[m * ld + K + j] = XU[m * rank + j];
-        } else {
-            const int64_t e = i - totalA;
-            const int64_t n = e / rank;
-            const int j = static_cast<int>(e - n * rank);
-            B[n * ld + K + j] = V[static_cast<int64_t>(j) * N + n];
-        }
+        const int64_t n = i / rank;
+        const int j = static_cast<int>(i - n * rank);
+        Vt[i] = V[static_cast<int64_t>(j) * N + n];
     }
 }
 
@@ -244,41 +222,99 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
               const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
               const uint16_t* V, int64_t rank, const uint16_t* bias, uint16_t* Y, int64_t ldy,
               void* ws, size_t ws_bytes, void* stream) {
-    if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX - 64)
+    if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return QG_ERR_INVALID_ARG;
     if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;
     if (K % kW4A4Block) return QG_ERR_INVALID_ARG;
     if (rank != 0 && rank != kW4A4MaxRank) return QG_ERR_UNSUPPORTED;
     if (!Xq || !Xscale || !Wq || !Wscale || !Y || (rank && (!XU || !V))) return QG_ERR_INVALID_ARG;
     if (ldy < N) return QG_ERR_INVALID_ARG;
-    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(Y)) return QG_ERR_MISALIGNED;
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(Y) || (rank && !aligned16(XU)))
+        return QG_ERR_MISALIGNED;
     const size_t need = qg_workspace_size(QG_OP_W4A4, M, N, K);
     if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return QG_ERR_MISALIGNED;
     const int dev = current_device();
-    if (dev < 0) return QG_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
     Ctl ctl = host_ctl(dev);
     if (!ctl.status) return QG_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const int64_t ke = K + rank;  // multiple of 32 halves: 16-byte aligned rows
-    __half* A16 = static_cast<__half*>(ws);
-    __half* B16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
-                                            ((static_cast<size_t>(M) * ke * 2 + 255) & ~size_t(255)));
-    k_w4a4_fold<<<conv_grid(dev, M * K / 16), 256, 0, s>>>(M, static_cast<int>(K), Xq,
-                                                           reinterpret_cast<const __half*>(Xscale),
-                                                           A16, ke);
-    k_w4a4_fold<<<conv_grid(dev, N * K / 16), 256, 0, s>>>(N, static_cast<int>(K), Wq,
-                                                           reinterpret_cast<const __half*>(Wscale),
-                                                           B16, ke);
-    if (rank)
-        k_w4a4_lowrank_cols<<<conv_grid(dev, (M + N) * rank), 256, 0, s>>>(
-            static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), static_cast<int>(rank),
-            reinterpret_cast<const __half*>(XU), reinterpret_cast<const __half*>(V), A16, B16, ke);
-    int rc = map_cuda(cudaGetLastError());
+    auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    const int nblk = static_cast<int>(K / kW4A4Block);
+    const int64_t Mp = (M + 3) & ~int64_t(3), Np = (N + 3) & ~int64_t(3);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint8_t* A8 = base;
+    uint8_t* B8 = A8 + up(static_cast<size_t>(M) * K);
+    float* SXt = reinterpret_cast<float*>(B8 + up(static_cast<size_t>(N) * K));
+    float* SWt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(SXt) +
+                                          up(4ull * (nblk + 1) * Mp));
+    __half* Vt = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(SWt) +
+                                           up(4ull * (nblk + 1) * Np));
+
+    int rc = s4_to_e4m3(Xq, M, K, K / 2, A8, K, dev, s);
+    if (!rc) rc = s4_to_e4m3(Wq, N, K, K / 2, B8, K, dev, s);
     if (rc) return rc;
-    return run_gemm_f16_tc(A16, ke, B16, ke, M, N, ke, reinterpret_cast<__half*>(Y), ldy,
-                           reinterpret_cast<const __half*>(bias), ctl, s);
+    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
+        M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), SXt);
+    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
+        N, Np, nblk, reinterpret_cast<const __half*>(Wscale), SWt);
+    if (rank)
+        k_transpose_v<<<conv_grid(dev, N * rank), 256, 0, s>>>(
+            static_cast<int>(N), static_cast<int>(rank), reinterpret_cast<const __half*>(V), Vt);
+    rc = map_cuda(cudaGetLastError());
+    if (rc) return rc;
+
+    using Cfg = W4A4Cfg;
+    CUtensorMap tA, tB, tXU, tVt, tSX, tSW;
+    rc = make_tmap_kmajor(&tA, false, A8, K, M, K, Cfg::BK, Cfg::BM);
+    if (!rc) rc = make_tmap_kmajor(&tB, false, B8, K, N, K, Cfg::BK, Cfg::BN);
+    if (!rc) rc = make_tmap_2d(&tSX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SXt, Mp, nblk + 1, Mp * 4,
+                               Cfg::BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!rc) rc = make_tmap_2d(&tSW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SWt, Np, nblk + 1, Np * 4,
+                               Cfg::BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rank) {
+        // 32 low-rank columns in a 64-wide (128-byte) box: TMA zero-fills the rest
+        if (!rc) rc = make_tmap_kmajor(&tXU, true, XU, rank, M, rank * 2, 64, Cfg::BM);
+        if (!rc) rc = make_tmap_kmajor(&tVt, true, Vt, rank, N, rank * 2, 64, Cfg::BN);
+    } else {
+        tXU = tA;  // never read without the low-rank unit
+        tVt = tB;
+    }
+    if (rc) return rc;
+
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    W4A4Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_ks = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
+    p.nblk = nblk;
+    p.lowrank = rank ? 1 : 0;
+    p.Y = reinterpret_cast<__half*>(Y);
+    p.ldy = ldy;
+    p.bias = reinterpret_cast<const __half*>(bias);
+    p.ctl = ctl;
+    const int64_t tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
+    const int grid = static_cast<int>(tiles < num_sms(dev) ? tiles : num_sms(dev));
+    void *pb = nullptr, *pa = nullptr;
+    profile_events(&pb, &pa);
+    if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), s) != cudaSuccess) return QG_ERR_CUDA;
+    w4a4_gemm_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tA, tB, tXU, tVt, tSX, tSW, p);
+    rc = map_cuda(cudaGetLastError());
+    if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), s) != cudaSuccess)
+        return QG_ERR_CUDA;
+    return rc;
 }
 
 }  // extern "C"

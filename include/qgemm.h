@@ -79,6 +79,11 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K);
  * call gave up on a bounded wait.  A failed CUDA call returns QG_ERR_CUDA. */
 int qg_device_status(void *stream);
 
+/* Diagnostics: the code of the most recent failed CUDA call behind a
+ * QG_ERR_CUDA (a cudaError_t, or minus a CUresult for a driver call such as
+ * the tensor-map encoder), 0 if none; reading it clears it. */
+int qg_last_cuda_error(void);
+
 /* Sets the limit of every device-side wait, in nanoseconds (default 2e9;
  * also read once from the environment variable QG_TIMEOUT_NS).  0 restores
  * the default. */
@@ -96,6 +101,13 @@ int qg_set_s8_chunk(int kblocks);
  * the kernel launched just before it on the same stream; pass 0 to turn the
  * overlap off. */
 int qg_set_pdl(int enable);
+
+/* Measurement hook: while `before` and `after` are non-NULL cudaEvent_t
+ * handles (created by the caller), every qgemm_s8, qgemm_s4, gemm_f16 and
+ * w4a4_gemm call records `before` on its stream right before launching its
+ * tensor-core GEMM kernel and `after` right after it, so that kernel can be
+ * timed alone.  Pass NULL, NULL to stop.  Both or neither must be NULL. */
+int qg_set_profile_events(void *before, void *after);
 
 /* [L4] Exact INT8 GEMM:  C[i][j] = sum_k A[i][k] * B[j][k]  (int32 result).
  *  A : int8, M x K row-major, lda >= K.
