@@ -57,6 +57,7 @@ SIGNATURES = {
     "qg_set_pdl": (_int, [_int]),
     "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
+    "qgemm_s8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),
     "qgemm_s4": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "gemm_f16": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),
     "w4a16_gemm": (_int, [_i64, _i64, _i64, _p, _i64, _p, _p, _i64, _p, _i64, _p]),

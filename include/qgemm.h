@@ -123,6 +123,30 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K,
              int32_t *C, int64_t ldc,
              void *ws, size_t ws_bytes, void *stream);
 
+/* qgemm_s8 without a caller-supplied workspace.  The paper has no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory: plugin hosts that pass a kernel only its inputs and outputs
+ * and own every allocation, engines whose memory plan is fixed after
+ * start-up, and code that must not call cudaMalloc at that point (it can
+ * synchronize the device).  Arguments, layouts and results are those of
+ * qgemm_s8.  The scratch is a static device array of
+ * QG_S8_NOALLOC_SCRATCH_BYTES inside this library, held by every GPU that
+ * loads the library until the process exits:
+ *  - problems needing more than that (qg_workspace_size(QG_OP_S8, M, N, K)
+ *    > QG_S8_NOALLOC_SCRATCH_BYTES, e.g. beyond M = N = K = 2048) return
+ *    QG_ERR_WORKSPACE and enqueue nothing;
+ *  - the first call on each device looks up the array's device address with
+ *    that device current; make it before any stream capture on the device;
+ *  - all calls share the array and it keeps the last call's contents; no part
+ *    of it needs to start at zero, but calls that overlap on the GPU (other
+ *    streams, unordered host threads) race on it: serialize them.
+ * It calls no allocator. */
+#define QG_S8_NOALLOC_SCRATCH_BYTES (16u << 20)
+int qgemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
+                     const int8_t *A, int64_t lda, int layout_a,
+                     const int8_t *B, int64_t ldb, int layout_b,
+                     int32_t *C, int64_t ldc, void *stream);
+
 /* [L4] Exact INT4 GEMM on s4p operands:  C = A . B^T  (int32 result).
  *  A : s4p, M x K values, lda_bytes >= K/2.
  *  B : s4p, K-major (N x K values), ldb_bytes >= K/2.
