@@ -50,6 +50,12 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
     return v;
 }
 
+__device__ __forceinline__ unsigned short ld_nc_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1) {
     asm volatile(
@@ -202,6 +208,216 @@ __global__ void __launch_bounds__(kW16Threads)
     }
 }
 
+// ---------------------------------------------------------------- decode
+//
+// Decode shapes (M <= 16) compute Y^T = W . X^T: the weights are the MMA's A
+// operand (16 weight rows per m16n8k16) and X^T the B operand (8 batch rows
+// per MMA), so a batch of one wastes 7/8 of an MMA instead of 15/16.
+//
+// In a chain of layers a call can only use X once the previous call has
+// finished, so everything that does not need X comes first:
+//  - at entry one thread bulk-copies the CTA's 16 weight rows into shared
+//    memory (cp.async.bulk: a few large transfers, the whole slab in flight
+//    at once), before the previous kernel has finished;
+//  - after griddepcontrol.wait each warp stages only its own K slice of X,
+//    already regrouped into the pair order the MMA fragments use, so the
+//    inner loop reads a fragment with one 16-byte shared load.
+// The per-weight work is the dequantization, exact in fp16: one lop3 per
+// fp16 pair does the two's-complement fix (XOR 8), the mask and the exponent
+// OR at once; even k gives 1024 + (v + 8) (minus 1032 -> v), odd k gives
+// 1024 + 16 (v + 8) (times 1/16 minus 72 -> v).  Group scales are applied
+// in fp32 after each group's MMAs.  CTA: one 16-row weight tile, 8 warps,
+// warp w on K slice w; partial tiles are added through shared memory.
+constexpr int kXRowPad = 32;
+constexpr int kWRowPad = 64;
+constexpr size_t kDecMaxSmem = 200 * 1024;  // dynamic shared memory for weights + X
+constexpr int kSiteW16Bulk = 301;
+constexpr int kSiteW16Drain = 302;
+
+__device__ __forceinline__ int xs_swizzle(int chunk) { return chunk ^ ((chunk >> 3) & 1); }
+
+// Weights: 16 rows of K/2 bytes (+ pad).  X: 8 warp slices of M rows, each
+// ceil(G/8) groups of 128 halves (+ pad).
+__host__ __device__ constexpr size_t dec_smem_bytes(int64_t M, int64_t K) {
+    return 16 * static_cast<size_t>(K / 2 + kWRowPad) +
+           8 * static_cast<size_t>(M) * (256 * static_cast<size_t>((K / 128 + 7) / 8) + kXRowPad);
+}
+
+// d = b ? (c ? ~a : a) : c, bitwise: with b = mask and c = (exponent bits
+// outside the mask) | (8-bits inside it), one instruction XORs the nibbles
+// with 8, keeps them and ORs in the fp16 exponent.
+__device__ __forceinline__ uint32_t lop3_nib(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Exact fp16 pairs of the 8 signed nibbles of `w` (nibble j = physical k_j):
+// p[0] = (k0, k4), p[1] = (k1, k5), p[2] = (k2, k6), p[3] = (k3, k7).
+__device__ __forceinline__ void dequant_word_fast(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t e0 = lop3_nib(w, 0x000F000Fu, 0x64086408u);   // 1024 + n ^ 8
+    const uint32_t e1 = lop3_nib(w, 0x00F000F0u, 0x64806480u);   // 1024 + 16 (n ^ 8)
+    const uint32_t e2 = lop3_nib(w8, 0x000F000Fu, 0x64086408u);
+    const uint32_t e3 = lop3_nib(w8, 0x00F000F0u, 0x64806480u);
+    const __half2 c1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 c16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    const __half2 cm72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+    __half2 v0 = __hsub2(*reinterpret_cast<const __half2*>(&e0), c1032);
+    __half2 v1 = __hfma2(*reinterpret_cast<const __half2*>(&e1), c16th, cm72);
+    __half2 v2 = __hsub2(*reinterpret_cast<const __half2*>(&e2), c1032);
+    __half2 v3 = __hfma2(*reinterpret_cast<const __half2*>(&e3), c16th, cm72);
+    p[0] = *reinterpret_cast<uint32_t*>(&v0);
+    p[1] = *reinterpret_cast<uint32_t*>(&v1);
+    p[2] = *reinterpret_cast<uint32_t*>(&v2);
+    p[3] = *reinterpret_cast<uint32_t*>(&v3);
+}
+
+template <int MB>  // batch tiles of 8 rows: M <= 8 * MB
+__global__ void __launch_bounds__(kW16Threads, 2)
+    k_w4a16_dec(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
+                const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
+                int64_t ldy, const Ctl ctl) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ float red[8][MB * 4][32];
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int failed;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup;
+    const int gpw = (G + 7) / 8;
+    const int gbeg = min(G, warp * gpw), gend = min(G, gbeg + gpw);
+    const int n0 = blockIdx.x * 16;
+    const int rows = min(16, N - n0);
+    const int wrs = K / 2 + kWRowPad;          // bytes per staged weight row
+    const int xrs = 256 * gpw + kXRowPad;      // bytes per staged X row of one warp's slice
+    uint8_t* ws = dsm;
+    uint8_t* xw = dsm + 16 * wrs + warp * M * xrs;  // this warp's X slice
+    const uint32_t bar = smem_u32(&wbar);
+
+    if (threadIdx.x == 0) {
+        failed = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // one row per lane, issued in parallel
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * (K / 2));
+        __syncwarp();
+        if (lane < rows)
+            bulk_copy_g2s(smem_u32(ws + lane * wrs), Wq + static_cast<int64_t>(n0 + lane) * (K / 2),
+                          static_cast<uint32_t>(K / 2), bar);
+    }
+    pdl_launch_dependents();
+
+    // Scales stay raw 16-bit until used.
+    unsigned short s0[8], s1[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const int gi = gbeg + b;
+        s0[b] = (gi < gend && g < rows) ? ld_nc_u16(S + static_cast<int64_t>(n0 + g) * G + gi) : 0;
+        s1[b] = (gi < gend && g + 8 < rows) ? ld_nc_u16(S + static_cast<int64_t>(n0 + g + 8) * G + gi)
+                                            : 0;
+    }
+
+    // X may be the previous kernel's output: stage this warp's slice only now,
+    // each 8-k chunk as the pairs (x0,x4), (x1,x5), (x2,x6), (x3,x7).
+    pdl_wait_prior_grid();
+    {
+        const int kbase = gbeg * kGroup;
+        const int cpr = (gend - gbeg) * (kGroup / 8);  // 16-byte chunks per row of the slice
+        for (int c = lane; c < M * cpr; c += 32) {
+            const int r = c / cpr, cc = c - r * cpr;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + r * ldx + kbase + cc * 8));
+            const uint4 o = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                                       __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+            *reinterpret_cast<uint4*>(xw + r * xrs + xs_swizzle(cc) * 16) = o;
+        }
+        __syncwarp();
+    }
+    if (!bounded_wait(bar, 0u, nullptr, ctl, kSiteW16Bulk)) {
+        failed = 1;
+        if (lane == 0) bounded_wait(bar, 0u, nullptr, ctl, kSiteW16Drain);
+    }
+
+    float acc[MB][4];
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mb][i] = 0.f;
+
+    for (int gb = gbeg; gb < gend; gb += 8) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int gi = gb + b;
+            if (gi >= gend) break;
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u);  // nibbles 0: rows past N contribute 0
+            uint4 w1 = w0;
+            if (g < rows) w0 = *reinterpret_cast<const uint4*>(ws + g * wrs + gi * 64 + 16 * t);
+            if (g + 8 < rows)
+                w1 = *reinterpret_cast<const uint4*>(ws + (g + 8) * wrs + gi * 64 + 16 * t);
+            float tmp[MB][4];
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tmp[mb][i] = 0.f;
+            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t pa[4], pb[4];
+                dequant_word_fast(wa[i], pa);
+                dequant_word_fast(wb[i], pb);
+                const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+                const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+                const int chunk = ((gi - gbeg) * kGroup + 32 * t + 8 * i) >> 3;
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb) {
+                    const int m = mb * 8 + g;
+                    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                    if (m < M) xv = *reinterpret_cast<const uint4*>(xw + m * xrs + xs_swizzle(chunk) * 16);
+                    mma_16816(tmp[mb], a0, xv.x, xv.y);
+                    mma_16816(tmp[mb], a1, xv.z, xv.w);
+                }
+            }
+            const float sc0 = __half2float(__ushort_as_half(s0[(gi - gbeg) & 7]));
+            const float sc1 = __half2float(__ushort_as_half(s1[(gi - gbeg) & 7]));
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+                acc[mb][0] = fmaf(tmp[mb][0], sc0, acc[mb][0]);
+                acc[mb][1] = fmaf(tmp[mb][1], sc0, acc[mb][1]);
+                acc[mb][2] = fmaf(tmp[mb][2], sc1, acc[mb][2]);
+                acc[mb][3] = fmaf(tmp[mb][3], sc1, acc[mb][3]);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[warp][mb * 4 + i][lane] = acc[mb][i];
+    __syncthreads();
+    if (warp >= MB || failed) return;
+    // warp mb writes batch tile mb: lane (g, t) holds Y[mb*8 + 2t + {0,1}][n0 + g / n0 + g + 8]
+    const int mb = warp;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += red[q][mb * 4 + i][lane];
+        v[i] = sum;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int m = mb * 8 + 2 * t + j;
+        if (m >= M) continue;
+        if (g < rows) Y[m * ldy + n0 + g] = __float2half_rn(v[j]);
+        if (g + 8 < rows) Y[m * ldy + n0 + g + 8] = __float2half_rn(v[2 + j]);
+    }
+}
+
 static std::atomic<int> g_w4a16_pdl{1};
 
 template <int MT, int NT>
@@ -218,6 +434,30 @@ static int launch_w4a16(int M, int N, int K, const __half* X, int64_t ldx, const
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16<MT, NT>, M, N, K, X, ldx, Wq, S, Y, ldy));
+}
+
+template <int MB>
+static int launch_w4a16_dec(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
+                            const __half* S, __half* Y, int64_t ldy, size_t smem, const Ctl& ctl,
+                            cudaStream_t s) {
+    static std::atomic<int> attr_done{0};
+    if (smem > 48 * 1024 && !attr_done.load()) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            k_w4a16_dec<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDecMaxSmem));
+        if (e != cudaSuccess) return map_cuda(e);
+        attr_done.store(1);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + 15) / 16));
+    cfg.blockDim = dim3(kW16Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_dec<MB>, M, N, K, X, ldx, Wq, S, Y, ldy, ctl));
 }
 
 }  // namespace qg
@@ -247,6 +487,20 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
     const __half* Sh = reinterpret_cast<const __half*>(Wscale);
     __half* Yh = reinterpret_cast<__half*>(Y);
     const int n = static_cast<int>(N), k = static_cast<int>(K);
+    // Decode shapes: weight slab bulk-copied and X staged in shared memory,
+    // weights as the A operand.
+    const size_t dec_smem = dec_smem_bytes(M, K);
+    if (M <= 16 && dec_smem <= kDecMaxSmem) {
+        const int dev = current_device();
+        if (dev < 0) return QG_ERR_CUDA;
+        const Ctl ctl = host_ctl(dev);
+        if (!ctl.status) return QG_ERR_CUDA;
+        if (M <= 8)
+            return launch_w4a16_dec<1>(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy,
+                                       dec_smem, ctl, s);
+        return launch_w4a16_dec<2>(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy, dec_smem,
+                                   ctl, s);
+    }
     // Rows are processed in chunks of up to 128 (8 m16 tiles per CTA).
     for (int64_t r0 = 0; r0 < M; r0 += 128) {
         const int m = static_cast<int>(M - r0 < 128 ? M - r0 : 128);
