@@ -54,6 +54,7 @@ SIGNATURES = {
     "qg_last_cuda_error": (_int, []),
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
     "qg_set_s8_chunk": (_int, [_int]),
+    "qg_set_gemm_path": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
     "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),

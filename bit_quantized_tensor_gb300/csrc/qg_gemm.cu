@@ -18,7 +18,7 @@
 #include <mutex>
 
 #include "qg_gemm_host.h"
-#include "tc_gemm.cuh"
+#include "tc_gemm2.cuh"
 
 namespace qg {
 
@@ -123,11 +123,81 @@ static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ld
     return rc;
 }
 
+// Paired-CTA version (cta_group::2, 256 x 256 tiles per SM pair).
+template <class Cfg>
+static int launch_tc2(const void* A, int64_t lda_bytes, const void* B, int64_t ldb_bytes, int64_t M,
+                      int64_t N, int64_t K, void* C, int64_t ldc, int chunk_kb, const __half* bias,
+                      const Ctl& ctl, cudaStream_t stream) {
+    constexpr bool f16 = Cfg::KIND == MmaKind::F16;
+    CUtensorMap ta, tb;
+    int rc = make_tmap_kmajor(&ta, f16, A, K, M, lda_bytes, Cfg::BK, Cfg::BM);
+    if (rc) return rc;
+    rc = make_tmap_kmajor(&tb, f16, B, K, N, ldb_bytes, Cfg::BK, Cfg::B_ROWS);
+    if (rc) return rc;
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(tc_gemm2_kernel<Cfg>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    TcGemmParams p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
+    p.chunk_kb = chunk_kb > 0 ? chunk_kb : p.num_kb;
+    p.C = C;
+    p.ldc = ldc;
+    p.bias = bias;
+    p.ctl = ctl;
+    const int64_t tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
+    const int64_t max_pairs = num_sms(dev) / 2;
+    const int grid = 2 * static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    void *pb = nullptr, *pa = nullptr;
+    profile_events(&pb, &pa);
+    if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), stream) != cudaSuccess) return QG_ERR_CUDA;
+    tc_gemm2_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
+    rc = map_cuda(cudaGetLastError());
+    if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), stream) != cudaSuccess)
+        return QG_ERR_CUDA;
+    return rc;
+}
+
+// GEMM kernel choice: 0 = by shape (pairs when M >= 256 and N >= 256),
+// 1 = always one CTA per tile, 2 = always CTA pairs.  Testing hook.
+static std::atomic<int> g_gemm_path{0};
+
+static bool use_pairs(int64_t M, int64_t N) {
+    const int path = g_gemm_path.load();
+    if (path == 1) return false;
+    if (path == 2) return true;
+    return M >= 256 && N >= 256;
+}
+
+template <MmaKind KIND, Epi EPI>
+static int launch_gemm(const void* A, int64_t lda_bytes, const void* B, int64_t ldb_bytes, int64_t M,
+                       int64_t N, int64_t K, void* C, int64_t ldc, int chunk_kb, const __half* bias,
+                       const Ctl& ctl, cudaStream_t stream) {
+    if (use_pairs(M, N))
+        return launch_tc2<Tc2Cfg<KIND, EPI>>(A, lda_bytes, B, ldb_bytes, M, N, K, C, ldc, chunk_kb,
+                                            bias, ctl, stream);
+    return launch_tc<TcGemmCfg<KIND, EPI>>(A, lda_bytes, B, ldb_bytes, M, N, K, C, ldc, chunk_kb,
+                                          bias, ctl, stream);
+}
+
 int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, int64_t M, int64_t N,
                     int64_t K, __half* C, int64_t ldc, const __half* bias, const Ctl& ctl,
                     cudaStream_t stream) {
-    using Cfg = TcGemmCfg<MmaKind::F16, Epi::F16>;
-    return launch_tc<Cfg>(A, lda * 2, B, ldb * 2, M, N, K, C, ldc, 0, bias, ctl, stream);
+    return launch_gemm<MmaKind::F16, Epi::F16>(A, lda * 2, B, ldb * 2, M, N, K, C, ldc, 0, bias, ctl,
+                                               stream);
 }
 
 // -------------------------------------------------------- operand converters
@@ -234,6 +304,12 @@ int qg_set_profile_events(void* before, void* after) {
     return QG_OK;
 }
 
+int qg_set_gemm_path(int path) {
+    if (path < 0 || path > 2) return QG_ERR_INVALID_ARG;
+    g_gemm_path.store(path);
+    return QG_OK;
+}
+
 int qg_set_s8_chunk(int kblocks) {
     if (kblocks < 1 || kblocks > 16) return QG_ERR_INVALID_ARG;
     g_s8_chunk_kb = kblocks;
@@ -285,8 +361,8 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, int 
     k_s8_to_f16<<<conv_grid(dev, N * K / 16), 256, 0, s>>>(B, N, K, ldb, B16, K);
     int rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
-    using Cfg = TcGemmCfg<MmaKind::F16, Epi::S32>;
-    return launch_tc<Cfg>(A16, K * 2, B16, K * 2, M, N, K, C, ldc, g_s8_chunk_kb, nullptr, ctl, s);
+    return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc,
+                                               g_s8_chunk_kb, nullptr, ctl, s);
 }
 
 int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_bytes, int layout_a,
@@ -314,9 +390,8 @@ int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_byte
     k_s4_to_e4m3<<<conv_grid(dev, N * K / 32), 256, 0, s>>>(B, N, K / 2, ldb_bytes, B8, K);
     int rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
-    using Cfg = TcGemmCfg<MmaKind::F8F6F4, Epi::S32>;
     // Partial sums are bounded by 64*K < 2^24: one accumulation unit per tile.
-    return launch_tc<Cfg>(A8, K, B8, K, M, N, K, C, ldc, 0, nullptr, ctl, s);
+    return launch_gemm<MmaKind::F8F6F4, Epi::S32>(A8, K, B8, K, M, N, K, C, ldc, 0, nullptr, ctl, s);
 }
 
 }  // extern "C"

@@ -94,6 +94,12 @@ int qg_set_timeout_ns(uint64_t ns);
  * value in 1..16; shorter chunks only cost more accumulator drains. */
 int qg_set_s8_chunk(int kblocks);
 
+/* Testing hook: tensor-core GEMM kernel of gemm_f16, qgemm_s8 and qgemm_s4.
+ * 0 = chosen by shape (CTA pairs with 256 x 256 tiles when M >= 256 and
+ * N >= 256, else one CTA per 128 x 256 tile), 1 = always one CTA per tile,
+ * 2 = always CTA pairs.  Results are identical; only speed differs. */
+int qg_set_gemm_path(int path);
+
 /* Programmatic dependent launch of w4a16_gemm (default on).  When on, a
  * w4a16_gemm kernel may start while the previous kernel on the stream is
  * still running: it streams Wq and Wscale at once and reads X only after

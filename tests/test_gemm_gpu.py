@@ -205,3 +205,51 @@ def test_qgemm_s4_sweep_large(dev, oracle, n):
     ref = oracle.gemm_s4(A[rows], B, n)
     assert np.array_equal(C[rows], ref), first_mismatch(C[rows], ref)
     freivalds_int(oracle.s4_unpack(A, n), oracle.s4_unpack(B, n), C)
+
+
+# ------------------------------------------- both tensor-core kernel paths
+
+@pytest.fixture
+def gemm_path():
+    import bit_quantized_tensor_gb300 as qg
+    def set_path(p):
+        assert qg.lib().qg_set_gemm_path(p) == 0
+    yield set_path
+    qg.lib().qg_set_gemm_path(0)
+
+
+PATH_SHAPES = [(1, 1, 32), (300, 300, 1056), (257, 520, 96), (520, 260, 2112), (256, 256, 64),
+               (640, 1000, 512)]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K", PATH_SHAPES)
+def test_paths_qgemm_s8(dev, oracle, gemm_path, path, M, N, K):
+    gemm_path(path)
+    A = inputs.s8_uniform(M, K, 1500 + M)
+    B = inputs.s8_uniform(N, K, 2500 + N)
+    C = _s8(dev, A, B)
+    ref = oracle.gemm_s8(A, B)
+    assert np.array_equal(C, ref), first_mismatch(C, ref)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K", PATH_SHAPES)
+def test_paths_qgemm_s4(dev, oracle, gemm_path, path, M, N, K):
+    gemm_path(path)
+    A = inputs.s4_packed_uniform(M, K, 1600 + M)
+    B = inputs.s4_packed_uniform(N, K, 2600 + N)
+    C = _s4(dev, A, B, K)
+    ref = oracle.gemm_s4(A, B, K)
+    assert np.array_equal(C, ref), first_mismatch(C, ref)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K", PATH_SHAPES)
+def test_paths_gemm_f16(dev, oracle, gemm_path, path, M, N, K):
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    A = inputs.f16_normal(M, K, 1700 + M)
+    B = inputs.f16_normal(N, K, 2700 + N)
+    C = qg.gemm_f16(_t(A, dev), _t(B, dev)).cpu().numpy()
+    assert_fp16_close(C, oracle.gemm_f16(A, B), f"gemm_f16 path {path} {M}x{N}x{K}")
