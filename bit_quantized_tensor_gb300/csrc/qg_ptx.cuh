@@ -79,9 +79,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Returns false (after recording QG_ERR_TIMEOUT with the call-site tag) when
 // the limit runs out, or when another role of this CTA has already set
 // `*abort_flag`.  `abort_flag` may be null (drain waits ignore aborts).
-static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          const Ctl& ctl, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t parity,
+                                                      volatile int* abort_flag, const Ctl& ctl,
+                                                      int site) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < kMaxWaitIterations; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -93,6 +93,13 @@ static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity, 
     if (abort_flag) *abort_flag = 1;
     report_error(ctl, QG_ERR_TIMEOUT, site);
     return false;
+}
+
+// Inline fast path: one try_wait; the bounded loop only when not yet ready.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             const Ctl& ctl, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return bounded_wait_slow(bar, parity, abort_flag, ctl, site);
 }
 
 // -------------------------------------------------------------------- TMA

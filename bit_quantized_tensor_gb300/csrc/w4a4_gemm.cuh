@@ -19,9 +19,9 @@
 //
 // Three rings advance independently ("three independent pipelines: main
 // operands, low-rank branch, drain"):
-//   operand ring   STAGES x (A 128x128 B, B 256x128 B), TMA -> MMA
-//   scale ring     SC_STAGES x (sX 2x128, sW 2x256 fp32), TMA -> epilogue
-//   accumulators   2 TMEM buffers of 128 x 256 fp32, MMA -> epilogue
+//   operand ring   STAGES x (A 128x128 B, B 192x128 B), TMA -> MMA
+//   scale ring     SC_STAGES x (sX 2x128, sW 2x192 fp32), TMA -> epilogue
+//   accumulators   2 TMEM buffers of 128 x 192 fp32, MMA -> epilogue
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -47,14 +47,16 @@ __device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float 
 }
 
 struct W4A4Cfg {
-    static constexpr int BM = 128, BN = 256;
+    // N = 192 lets 12 epilogue warps (3 per TMEM lane quadrant, 64 columns
+    // each) hold their fp32 accumulators in registers within a 14-warp block.
+    static constexpr int BM = 128, BN = 192;
     static constexpr int ROW_BYTES = 128;                 // 128 e4m3 per stage row = 2 blocks
     static constexpr int BK = 128;
     static constexpr int QBLOCK = 64;                     // scale block along K
     static constexpr int A_BYTES = BM * ROW_BYTES;        // 16 KB
-    static constexpr int B_BYTES = BN * ROW_BYTES;        // 32 KB
+    static constexpr int B_BYTES = BN * ROW_BYTES;        // 24 KB
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = 5;
     static constexpr int SC_STAGES = 6;
     static constexpr int SX_BYTES = 2 * BM * 4;           // two blocks of row scales (fp32)
     static constexpr int SW_BYTES = 2 * BN * 4;           // two blocks of column scales
@@ -66,7 +68,8 @@ struct W4A4Cfg {
     static constexpr int SMEM_LIMIT = 232448;
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EPI_WARPS = 8;
+    static constexpr int EPI_WARPS = 12;
+    static constexpr int EPI_COLS = BN / 3;               // columns per epilogue warp
     static constexpr int THREADS = 32 * (2 + EPI_WARPS);
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * SC_STAGES + 2 * ACC_BUFS + 1;
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, BM, BN);  // e4m3 or f16 x2, f32 acc
@@ -76,6 +79,8 @@ struct W4A4Cfg {
     static_assert(NUM_BARRIERS * 8 + 8 <= BARRIER_BYTES, "barrier area too small");
     static_assert(ACC_BUFS * BN <= TMEM_COLS, "TMEM budget exceeded");
     static_assert(SC_BYTES % 128 == 0 && STAGE_BYTES % 1024 == 0, "alignment of ring slots");
+    static_assert(EPI_COLS % 16 == 0 && BN % 16 == 0 && BN <= 256, "epilogue column split");
+    static_assert(THREADS <= 512, "more than 16 warps would cap registers at 96");
 };
 
 struct W4A4Params {
@@ -274,8 +279,8 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int quad = warp & 3;
-        const int colhalf = (warp - 2) >> 2;
+        const int quad = warp & 3;               // TMEM lane quadrant of this warp
+        const int colpart = (warp - 2) >> 2;     // which third of the tile's columns
         PipeState<ACC> as;
         PipeState<SCS> ss;
         bool ok = true;
@@ -284,10 +289,10 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
             tile_coords(t, num_m, num_n, mb, nb);
             const int rloc = quad * 32 + lane;
             const int row = mb * Cfg::BM + rloc;
-            const int col0 = nb * Cfg::BN + colhalf * 128;
-            float acc[128];
+            const int col0 = nb * Cfg::BN + colpart * Cfg::EPI_COLS;
+            float acc[Cfg::EPI_COLS];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+            for (int i = 0; i < Cfg::EPI_COLS; ++i) acc[i] = 0.f;
             const int steps = p.num_ks + p.lowrank;
             for (int ks = 0; ok && ks < steps; ++ks) {
                 const int units = (ks == p.num_ks) ? 1 : 2;
@@ -308,11 +313,12 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                     }
                     tc_fence_after();
                     const float sx = sx_s[h * Cfg::BM + rloc];
-                    const float* swc = sw_s + h * Cfg::BN + colhalf * 128;
+                    const float* swc = sw_s + h * Cfg::BN + colpart * Cfg::EPI_COLS;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(as.index * Cfg::BN + colhalf * 128);
+                                           static_cast<uint32_t>(as.index * Cfg::BN +
+                                                                 colpart * Cfg::EPI_COLS);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < Cfg::EPI_COLS / 16; ++c) {
                         uint32_t r[16];
                         tmem_ld_32x32b_x16(taddr + 16u * c, r);
                         tmem_wait_ld();
@@ -340,8 +346,8 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
             }
             if (!ok) break;
             if (row < p.M)
-                store_row_f16<128>(p.Y + static_cast<int64_t>(row) * p.ldy + col0, col0, p.N, acc,
-                                   p.bias);
+                store_row_f16<Cfg::EPI_COLS>(p.Y + static_cast<int64_t>(row) * p.ldy + col0, col0, p.N,
+                                             acc, p.bias);
         }
     }
 
