@@ -158,8 +158,9 @@ class Workload:
         # W4A4: weights quantized once (outside any timed region)
         self.X4 = t(inputs.f32_normal(W4_M, W4_K, 1004))
         Wf = t(inputs.f32_normal(W4_N, W4_K, 2004))
-        self.U = t(inputs.f16_normal(W4_K, W4_R, 3004, sigma=0.02))
-        self.V = t(inputs.f16_normal(W4_R, W4_N, 3005, sigma=0.02))
+        # low-rank factors in linear-layer weight layout: Ut rank x K, Vt N x rank
+        self.Ut = t(inputs.f16_normal(W4_K, W4_R, 3004, sigma=0.02).T)
+        self.Vt = t(inputs.f16_normal(W4_R, W4_N, 3005, sigma=0.02).T)
         self.bias = t(inputs.f16_normal(1, W4_N, 3006, sigma=0.1)[0])
         self.qw, self.sw, _ = qg.w4a4_quantize(Wf)
         del Wf
@@ -202,12 +203,12 @@ class Workload:
         return self.w16_sets
 
     def w4a4_quant(self):
-        self.qg.w4a4_quantize(self.X4, self.U, out=self.q_out)
+        self.qg.w4a4_quantize(self.X4, self.Ut, out=self.q_out)
         return 1
 
     def w4a4_gemm(self):
         q, s, xu = self.q_out
-        self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, V=self.V, bias=self.bias,
+        self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, Vt=self.Vt, bias=self.bias,
                           Y=self.Y4, ws=self.ws_w4)
         return 4
 

@@ -220,17 +220,22 @@ def w4a16_gemm(X, Wq, Wscale, group: int = 128, Y=None, stream=None):
     return Y
 
 
-def w4a4_quantize(X, U=None, block: int = 64, out=None, stream=None):
-    """Returns (Xq M x K/2 uint8, Xscale M x K/block fp16, XU M x rank fp16 or None)."""
+def w4a4_quantize(X, Ut=None, block: int = 64, out=None, stream=None):
+    """Returns (Xq M x K/2 uint8, Xscale M x K/block fp16, XU M x rank fp16 or None).
+
+    Ut is the low-rank down-projection transposed (rank x K fp16, the weight
+    of a K -> rank linear layer); XU = X . Ut^T.
+    """
     torch = _torch()
     _cuda(X, torch.float32, "X")
     M, K = X.shape
     rank = 0
+    U = Ut
     if U is not None:
-        _cuda(U, torch.float16, "U")
-        if not U.is_contiguous() or U.shape[0] != K:
-            raise ValueError("U must be a contiguous K x rank fp16 matrix")
-        rank = U.shape[1]
+        _cuda(U, torch.float16, "Ut")
+        if not U.is_contiguous() or U.dim() != 2 or U.shape[1] != K:
+            raise ValueError("Ut must be a contiguous rank x K fp16 matrix")
+        rank = U.shape[0]
     if out is None:
         Xq = torch.empty((M, K // 2), dtype=torch.uint8, device=X.device)
         Xs = torch.empty((M, K // block), dtype=torch.float16, device=X.device)
@@ -243,9 +248,15 @@ def w4a4_quantize(X, U=None, block: int = 64, out=None, stream=None):
     return Xq, Xs, XU
 
 
-def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, V=None, bias=None, block: int = 64,
+def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, Vt=None, bias=None, block: int = 64,
               Y=None, ws=None, stream=None):
+    """Y = (Q(X).Q(W)^T) (.) scale + XU . Vt^T + bias, fp16 M x N.
+
+    Vt is the low-rank up-projection transposed (N x rank fp16, the weight of
+    a rank -> N linear layer).
+    """
     torch = _torch()
+    V = Vt
     _cuda(Xq, torch.uint8, "Xq")
     _cuda(Wq, torch.uint8, "Wq")
     _cuda(Xscale, torch.float16, "Xscale")
@@ -254,8 +265,10 @@ def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, V=None, bias=None, block:
     rank = 0
     if XU is not None:
         _cuda(XU, torch.float16, "XU")
-        _cuda(V, torch.float16, "V")
+        _cuda(V, torch.float16, "Vt")
         rank = XU.shape[1]
+        if not V.is_contiguous() or V.dim() != 2 or V.shape != (N, rank):
+            raise ValueError("Vt must be a contiguous N x rank fp16 matrix")
     if bias is not None:
         _cuda(bias, torch.float16, "bias")
     if Y is None:

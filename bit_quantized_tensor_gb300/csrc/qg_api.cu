@@ -104,11 +104,11 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
             return round_up256(2 * m * k) + round_up256(2 * n * k);
         case QG_OP_S4:  // e4m3 copies of both operands (exact for int4 values)
             return round_up256(m * k) + round_up256(n * k);
-        case QG_OP_W4A4: {  // e4m3 operands, transposed fp32 scale tables, V^T
+        case QG_OP_W4A4: {  // e4m3 operands, transposed fp32 scale tables
             const size_t nblk = k / 64 + 1;
             const size_t mp = (m + 3) & ~static_cast<size_t>(3), np = (n + 3) & ~static_cast<size_t>(3);
             return round_up256(m * k) + round_up256(n * k) + round_up256(4 * nblk * mp) +
-                   round_up256(4 * nblk * np) + round_up256(2 * n * 32);
+                   round_up256(4 * nblk * np);
         }
         default:
             return 0;

@@ -26,140 +26,293 @@ constexpr int kW4A4MaxRank = 32;
 
 // ------------------------------------------------ quantizer (+ X . U)
 //
-// CTA: 128 threads, 16 rows.  Thread (row r = tid/8, segment j = tid%8)
-// owns K positions [64*b + 8j, 64*b + 8j + 8) of every block b of its row:
-// it quantizes them (absmax shared by the 8 segment lanes of the row through
-// shuffles) and accumulates their contribution to all `rank` columns of XU;
-// the 8 segment partial sums are added at the end.  U is staged per block in
-// shared memory as fp32, double buffered, with its 16-byte chunks rotated by
-// the segment index so the 8 lanes of a row read distinct banks.
-constexpr int kQRows = 16;
-constexpr int kQThreads = 128;
+// CTA: 8 warps on one 16-row tile of X, warp w on K slice w (a contiguous
+// range of 64-element blocks).  Each warp streams its blocks through a
+// private kQStages-deep ring in shared memory: lane 0 loads a block as two
+// TMA boxes of 16 rows x 32 floats (128-byte rows, 128-byte swizzle) and the
+// warp waits on the stage's mbarrier.  Lane (g, t) owns rows g and g + 8 at
+// the 16 positions [16t, 16t + 16) of every block, read as four 16-byte
+// chunks; lanes t = 2, 3 take their chunks in the order 2, 3, 0, 1, which
+// together with the swizzle puts the eight lanes of every shared-memory
+// phase on distinct banks.  x[4i + j] is position 16t + 4 (i ^ 2 (t / 2)) + j.
+// Per row and block: absmax through two shuffles, s = fp16(max / 7), codes
+// q = clamp(rint(fl(x / s)), -8, 7) (codes_fast, codes_exact), the lane's 8
+// code bytes stored at once.
+// X . U on mma.sync m16n8k16 (X rounded to fp16, fp32 accumulation): in step
+// i the lane's chunk i is its A fragment (k slots 2t, 2t+1 <- its first two
+// values, 2t+8, 2t+9 <- the other two) and the B fragment holds U at the same
+// four positions, read from U stored rank x K (row 8n + g) with two 16-byte
+// loads per n-tile.  The eight slices' partial X . U tiles are added through
+// shared memory at the end.
+constexpr int kQWarps = 8;
+constexpr int kQThreads = 32 * kQWarps;
+constexpr int kQStages = 3;
+constexpr int kQStageBytes = 16 * kW4A4Block * 4;                        // 4 KiB: 16 rows x 64 fp32
+constexpr int kQSmemBytes = kQWarps * kQStages * kQStageBytes + 1024;    // + alignment slack
 
-__device__ __forceinline__ int u_swz(int k, int r) {  // rank r of K row k, rotated
-    return k * kW4A4MaxRank + ((r + 4 * (k >> 3)) & (kW4A4MaxRank - 1));
+__device__ __forceinline__ void mma_16816_q(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__global__ void __launch_bounds__(kQThreads)
-    k_w4a4_quantize(int M, int K, const float* __restrict__ X, int64_t ldx,
-                    const __half* __restrict__ U, int rank, uint8_t* __restrict__ Xq,
-                    __half* __restrict__ Xs, __half* __restrict__ XU) {
-    __shared__ __align__(16) float us[2][kW4A4Block * kW4A4MaxRank];
-    const int tid = threadIdx.x;
-    const int r = tid >> 3;                 // row within the CTA
-    const int seg = tid & 7;                // 8-element segment within a block
-    const int row = blockIdx.x * kQRows + r;
-    const bool live = row < M;
-    const int nblk = K / kW4A4Block;
-    const bool lowrank = rank > 0;
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
 
-    float acc[kW4A4MaxRank];
+// Codes of one lane-row: four 16-bit groups, group i holding the codes of the
+// lane's chunk i (x[4i + j] in nibble j).  The definition is
+// q = s == 0 ? 0 : clamp(rint(fl(x / s)), -8, 7) with s = fp16(max / 7).
+//
+// Exact slow form: the IEEE division itself.
+__device__ __forceinline__ void codes_exact(const float (&x)[16], float s, uint32_t (&grp)[4]) {
 #pragma unroll
-    for (int i = 0; i < kW4A4MaxRank; ++i) acc[i] = 0.f;
-
-    auto stage_u = [&](int b, int buf) {
-        // 64 x 32 fp16 = 256 chunks of 8 halves; 2 chunks per thread.
+    for (int c = 0; c < 4; ++c) {
+        uint32_t w = 0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int chunk = tid * 2 + c;
-            const int k = chunk >> 2;
-            const int r0 = (chunk & 3) * 8;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                U + static_cast<int64_t>(b * kW4A4Block + k) * kW4A4MaxRank + r0));
-            const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f = __half22float2(h[q]);
-                us[buf][u_swz(k, r0 + 2 * q)] = f.x;
-                us[buf][u_swz(k, r0 + 2 * q + 1)] = f.y;
-            }
-        }
-    };
-
-    if (lowrank) stage_u(0, 0);
-    for (int b = 0; b < nblk; ++b) {
-        const int buf = b & 1;
-        float x[8];
-        if (live) {
-            const float4* src =
-                reinterpret_cast<const float4*>(X + static_cast<int64_t>(row) * ldx + b * kW4A4Block +
-                                                seg * 8);
-            const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
-            x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-            x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-        // Absmax over the 64-element block (8 lanes x 8 values).
-        float a = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-        const __half sh = __float2half_rn(__fdiv_rn(a, 7.0f));
-        const float s = __half2float(sh);
-        uint32_t packed = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int j = 0; j < 4; ++j) {
             int q = 0;
-            if (s != 0.f) {
-                float t = rintf(__fdiv_rn(x[i], s));
-                t = fminf(fmaxf(t, -8.f), 7.f);
-                q = static_cast<int>(t);
+            if (s != 0.f)
+                q = static_cast<int>(fminf(fmaxf(rintf(__fdiv_rn(x[4 * c + j], s)), -8.f), 7.f));
+            w |= (static_cast<uint32_t>(q) & 0xFu) << (4 * j);
+        }
+        grp[c] = w;
+    }
+}
+
+// Fast form, y = fl(x * fl(1 / s)) instead of fl(x / s).  It is kept for a
+// row only when s is a normal fp16 value and no y is within 2^-17 of a
+// half-integer; then it gives the same codes:
+//  - a normal s is within a factor (1 +- 2^-11) of max / 7, so |x / s| and
+//    |y| stay below 7.004: rint never leaves [-7, 7] and the clamp is idle;
+//  - |y - x / s| <= |x / s| (2^-24 + 2^-24 + 2^-48) < 2^-20 and
+//    |fl(x / s) - x / s| <= 2^-22 below 8, so a y more than 2^-17 from every
+//    half-integer has fl(x / s) on the same side of each of them;
+//  - y + 1.5 * 2^23 rounds y to an integer with ties to even (the sum's ulp
+//    is 1 and 1.5 * 2^23 is even), and the sum's four low mantissa bits are
+//    that integer's two's-complement nibble;
+//  - d = y - rint(y) is exact and |d| <= 1/2; "near a tie" is
+//    |d| > 1/2 - 2^-17.
+// Returns true when the row needs the exact form.
+__device__ __forceinline__ bool codes_fast(const float (&x)[16], float r, uint32_t (&grp)[4]) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr float kNearTie = 0.5f - 0x1p-17f;
+    bool near = false;
+    uint32_t pair[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        uint32_t b[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float y = x[2 * p + e] * r;
+            const float tq = __fadd_rn(y, kMagic);
+            const float d = __fsub_rn(y, __fsub_rn(tq, kMagic));
+            near |= fabsf(d) > kNearTie;
+            b[e] = __float_as_uint(tq);
+        }
+        // low nibble <- b[0], high nibble <- b[1]
+        pair[p] = (b[0] & 0x0Fu) | ((b[1] << 4) & 0xF0u);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) grp[c] = __byte_perm(pair[2 * c], pair[2 * c + 1], 0x0040);
+    return near;
+}
+
+__device__ __forceinline__ float absmax16(const float (&x)[16]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(x[i]), fabsf(x[i + 8]));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
+    return fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3]));
+}
+
+// The lane's 8 code bytes in position order from its chunk groups (chunk
+// order 0..3, or 2, 3, 0, 1 when `swapped`).
+__device__ __forceinline__ uint2 code_bytes(const uint32_t (&grp)[4], bool swapped) {
+    const uint32_t lo = __byte_perm(grp[0], grp[1], 0x5410);
+    const uint32_t hi = __byte_perm(grp[2], grp[3], 0x5410);
+    return swapped ? make_uint2(hi, lo) : make_uint2(lo, hi);
+}
+
+template <bool LOWRANK>
+__global__ void __launch_bounds__(kQThreads, 2)
+    k_w4a4_quantize(const __grid_constant__ CUtensorMap tmX, int M, int K,
+                    const __half* __restrict__ Ut, uint8_t* __restrict__ Xq, __half* __restrict__ Xs,
+                    __half* __restrict__ XU, const Ctl ctl) {
+    extern __shared__ uint8_t qsmem_raw[];
+    __shared__ __align__(8) uint64_t full[kQWarps][kQStages];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = K / kW4A4Block;
+    const int bpw = (nblk + kQWarps - 1) / kQWarps;
+    const int bbeg = min(nblk, warp * bpw), bend = min(nblk, bbeg + bpw);
+    const int tile_row = blockIdx.x * 16;
+    const int row0 = tile_row + g, row1 = row0 + 8;
+    const bool live0 = row0 < M, live1 = row1 < M;
+    const bool swapped = t >= 2;  // chunk order 2, 3, 0, 1
+
+    // 1024-byte aligned ring (the 128-byte swizzle repeats every 1024 bytes)
+    const uint32_t ring_base =
+        ((smem_u32(qsmem_raw) + 1023u) & ~1023u) + warp * (kQStages * kQStageBytes);
+    uint8_t* const ring_gen = qsmem_raw + (ring_base - smem_u32(qsmem_raw));
+    const uint32_t bar0 = smem_u32(&full[warp][0]);
+    if (lane == 0) {
+        for (int s = 0; s < kQStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmX);
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int b, int st) {  // lane 0 only
+        const uint32_t bar = bar0 + 8 * st;
+        const uint32_t dst = ring_base + st * kQStageBytes;
+        mbar_arrive_expect_tx(bar, kQStageBytes);
+        tma_load_2d(dst, &tmX, b * kW4A4Block, tile_row, bar, pol);
+        tma_load_2d(dst + kQStageBytes / 2, &tmX, b * kW4A4Block + 32, tile_row, bar, pol);
+    };
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kQStages; ++i)
+            if (bbeg + i < bend) issue(bbeg + i, i);
+    }
+
+    // shared-memory offsets of the lane's chunk i in rows g and g + 8
+    uint32_t off[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int ch = 4 * (t & 1) + (i ^ (swapped ? 2 : 0));  // chunk within the 128-byte half-row
+        off[i] = (t >> 1) * (kQStageBytes / 2) + g * 128 + ((ch ^ g) << 4);
+    }
+
+    float acc[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+
+    int fail_b = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int b = bbeg; b < bend; ++b) {
+        uint4 u[4][2];
+        if constexpr (LOWRANK) {
+            // piece h ^ swapped of the lane's 32 bytes of U row 8n + g
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    u[n][h] = __ldg(reinterpret_cast<const uint4*>(
+                        Ut + static_cast<int64_t>(8 * n + g) * K + b * kW4A4Block + 16 * t +
+                        8 * (h ^ (swapped ? 1 : 0))));
+        }
+        if (!__all_sync(0xffffffffu, bounded_wait(bar0 + 8 * stage, phase, nullptr, ctl, 20))) {
+            fail_b = b;
+            break;
+        }
+        float x0[16], x1[16];
+        {
+            const uint8_t* st = ring_gen + stage * kQStageBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v0 = *reinterpret_cast<const float4*>(st + off[i]);
+                const float4 v1 = *reinterpret_cast<const float4*>(st + off[i] + 8 * 128);
+                x0[4 * i] = v0.x; x0[4 * i + 1] = v0.y; x0[4 * i + 2] = v0.z; x0[4 * i + 3] = v0.w;
+                x1[4 * i] = v1.x; x1[4 * i + 1] = v1.y; x1[4 * i + 2] = v1.z; x1[4 * i + 3] = v1.w;
             }
-            packed |= (static_cast<uint32_t>(q) & 0xFu) << (4 * i);
         }
-        if (live) {
-            *reinterpret_cast<uint32_t*>(Xq + static_cast<int64_t>(row) * (K / 2) + b * 32 + seg * 4) =
-                packed;
-            if (seg == 0) Xs[static_cast<int64_t>(row) * nblk + b] = sh;
+        __syncwarp();  // every lane has read the stage: refill it
+        if (lane == 0 && b + kQStages < bend) issue(b + kQStages, stage);
+        if (++stage == kQStages) {
+            stage = 0;
+            phase ^= 1u;
         }
-        if (lowrank) {
-            __syncthreads();                              // us[buf] complete
-            if (b + 1 < nblk) stage_u(b + 1, buf ^ 1);    // overlaps the FMAs below
+
+        // Per-row block absmax over the 4 lanes t of the row.
+        float m0 = absmax16(x0), m1 = absmax16(x1);
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+        const __half h0 = __float2half_rn(__fdiv_rn(m0, 7.0f));
+        const __half h1 = __float2half_rn(__fdiv_rn(m1, 7.0f));
+        const float s0 = __half2float(h0), s1 = __half2float(h1);
+        uint32_t q0[4], q1[4];
+        const bool slow0 = codes_fast(x0, __frcp_rn(s0), q0) || !(s0 >= 0x1p-14f);
+        const bool slow1 = codes_fast(x1, __frcp_rn(s1), q1) || !(s1 >= 0x1p-14f);
+        if (__any_sync(0xffffffffu, slow0 || slow1)) {  // rare: near a tie, or a tiny block
+            if (slow0) codes_exact(x0, s0, q0);
+            if (slow1) codes_exact(x1, s1, q1);
+        }
+        if (live0) {
+            *reinterpret_cast<uint2*>(Xq + static_cast<int64_t>(row0) * (K / 2) + b * 32 + 8 * t) =
+                code_bytes(q0, swapped);
+            if (t == 0) Xs[static_cast<int64_t>(row0) * nblk + b] = h0;
+        }
+        if (live1) {
+            *reinterpret_cast<uint2*>(Xq + static_cast<int64_t>(row1) * (K / 2) + b * 32 + 8 * t) =
+                code_bytes(q1, swapped);
+            if (t == 0) Xs[static_cast<int64_t>(row1) * nblk + b] = h1;
+        }
+        if constexpr (LOWRANK) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = seg * 8 + i;
-                const float* urow = &us[buf][k * kW4A4MaxRank];
-                const int rot = 4 * (k >> 3);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a0 = pack_f16x2(x0[4 * i], x0[4 * i + 1]);
+                const uint32_t a1 = pack_f16x2(x1[4 * i], x1[4 * i + 1]);
+                const uint32_t a2 = pack_f16x2(x0[4 * i + 2], x0[4 * i + 3]);
+                const uint32_t a3 = pack_f16x2(x1[4 * i + 2], x1[4 * i + 3]);
 #pragma unroll
-                for (int c = 0; c < kW4A4MaxRank; c += 4) {
-                    const float4 u = *reinterpret_cast<const float4*>(urow + ((c + rot) & 31));
-                    acc[c] = fmaf(x[i], u.x, acc[c]);
-                    acc[c + 1] = fmaf(x[i], u.y, acc[c + 1]);
-                    acc[c + 2] = fmaf(x[i], u.z, acc[c + 2]);
-                    acc[c + 3] = fmaf(x[i], u.w, acc[c + 3]);
+                for (int n = 0; n < 4; ++n) {
+                    const uint4& p = u[n][i >> 1];
+                    mma_16816_q(acc[n], a0, a1, a2, a3, (i & 1) ? p.z : p.x, (i & 1) ? p.w : p.y);
                 }
             }
-            __syncthreads();                              // us[buf] may be overwritten
         }
     }
-    if (lowrank) {
+    if (fail_b >= 0) {
+        // A load did not arrive in time (recorded): wait, bounded, for the
+        // loads still in flight, blocks [fail_b, fail_b + kQStages), before
+        // the ring is reused or the CTA's shared memory is released.
+        if (lane == 0)
+            for (int bb = fail_b; bb < min(bend, fail_b + kQStages); ++bb)
+                bounded_wait(bar0 + 8 * ((bb - bbeg) % kQStages), ((bb - bbeg) / kQStages) & 1, nullptr,
+                             ctl, 21);
+        __syncwarp();
+    }
+    if constexpr (LOWRANK) {
+        // warp w's 16 x 32 partial into its own (drained) ring, then warp 0 sums
+        float* red = reinterpret_cast<float*>(ring_gen);
 #pragma unroll
-        for (int i = 0; i < kW4A4MaxRank; ++i) {
-            acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
-            acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
-            acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 4);
-        }
-        if (live) {
-            // Lane `seg` writes ranks 4*seg .. 4*seg+3.
-            float o[4];
+        for (int n = 0; n < 4; ++n)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float v = 0.f;
+            for (int i = 0; i < 4; ++i) red[(4 * n + i) * 32 + lane] = acc[n][i];
+        __syncthreads();
+        if (warp == 0) {
+            const float* red0 = reinterpret_cast<const float*>(ring_gen);
 #pragma unroll
-                for (int c = 0; c < kW4A4MaxRank; ++c)
-                    if (c == 4 * seg + q) v = acc[c];
-                o[q] = v;
+            for (int n = 0; n < 4; ++n) {
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kQWarps; ++w)
+                        sum += red0[w * (kQStages * kQStageBytes / 4) + (4 * n + i) * 32 + lane];
+                    v[i] = sum;
+                }
+                // C fragment: (row g, cols 2t, 2t+1) and (row g+8, same cols) of n-tile n
+                const int col = 8 * n + 2 * t;
+                if (live0)
+                    *reinterpret_cast<uint32_t*>(XU + static_cast<int64_t>(row0) * kW4A4MaxRank + col) =
+                        pack_f16x2(v[0], v[1]);
+                if (live1)
+                    *reinterpret_cast<uint32_t*>(XU + static_cast<int64_t>(row1) * kW4A4MaxRank + col) =
+                        pack_f16x2(v[2], v[3]);
             }
-            __half2 h0 = __floats2half2_rn(o[0], o[1]);
-            __half2 h1 = __floats2half2_rn(o[2], o[3]);
-            uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t*>(&h0);
-            pk.y = *reinterpret_cast<uint32_t*>(&h1);
-            *reinterpret_cast<uint2*>(XU + static_cast<int64_t>(row) * kW4A4MaxRank + 4 * seg) = pk;
         }
     }
 }
@@ -178,17 +331,6 @@ __global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
         float v = 0.f;
         if (r < rows) v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
         St[i] = v;
-    }
-}
-
-// Vt[n][j] = V[j][n];  V: rank x N, Vt: N x rank.
-__global__ void k_transpose_v(int N, int rank, const __half* __restrict__ V, __half* __restrict__ Vt) {
-    const int64_t total = static_cast<int64_t>(N) * rank;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t n = i / rank;
-        const int j = static_cast<int>(i - n * rank);
-        Vt[i] = V[static_cast<int64_t>(j) * N + n];
     }
 }
 
@@ -211,10 +353,38 @@ int w4a4_quantize(int64_t M, int64_t K, const float* X, int64_t ldx, const uint1
         return QG_ERR_MISALIGNED;
     const int dev = current_device();
     if (dev < 0) return QG_ERR_CUDA;
-    const int grid = static_cast<int>((M + kQRows - 1) / kQRows);
-    k_w4a4_quantize<<<grid, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<int>(M), static_cast<int>(K), X, ldx, reinterpret_cast<const __half*>(U),
-        static_cast<int>(rank), Xq, reinterpret_cast<__half*>(Xscale), reinterpret_cast<__half*>(XU));
+    if (dev >= 64) return QG_ERR_CUDA;
+    {
+        static std::mutex mu;
+        static bool attr_set[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(k_w4a4_quantize<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_w4a4_quantize<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmemBytes);
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    Ctl ctl = host_ctl(dev);
+    if (!ctl.status) return QG_ERR_CUDA;
+    CUtensorMap tX;
+    // two boxes of 16 rows x 32 floats (128-byte rows) per 64-element block
+    int rc = make_tmap_2d(&tX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, X, K, M, ldx * 4, 32, 16,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    const int grid = static_cast<int>((M + 15) / 16);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rank)
+        k_w4a4_quantize<true><<<grid, kQThreads, kQSmemBytes, s>>>(
+            tX, static_cast<int>(M), static_cast<int>(K), reinterpret_cast<const __half*>(U), Xq,
+            reinterpret_cast<__half*>(Xscale), reinterpret_cast<__half*>(XU), ctl);
+    else
+        k_w4a4_quantize<false><<<grid, kQThreads, kQSmemBytes, s>>>(
+            tX, static_cast<int>(M), static_cast<int>(K), nullptr, Xq,
+            reinterpret_cast<__half*>(Xscale), nullptr, ctl);
     return map_cuda(cudaGetLastError());
 }
 
@@ -229,7 +399,7 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     if (rank != 0 && rank != kW4A4MaxRank) return QG_ERR_UNSUPPORTED;
     if (!Xq || !Xscale || !Wq || !Wscale || !Y || (rank && (!XU || !V))) return QG_ERR_INVALID_ARG;
     if (ldy < N) return QG_ERR_INVALID_ARG;
-    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(Y) || (rank && !aligned16(XU)))
+    if (!aligned16(Xq) || !aligned16(Wq) || !aligned16(Y) || (rank && (!aligned16(XU) || !aligned16(V))))
         return QG_ERR_MISALIGNED;
     const size_t need = qg_workspace_size(QG_OP_W4A4, M, N, K);
     if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE;
@@ -249,8 +419,6 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     float* SXt = reinterpret_cast<float*>(B8 + up(static_cast<size_t>(N) * K));
     float* SWt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(SXt) +
                                           up(4ull * (nblk + 1) * Mp));
-    __half* Vt = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(SWt) +
-                                           up(4ull * (nblk + 1) * Np));
 
     int rc = s4_to_e4m3(Xq, M, K, K / 2, A8, K, dev, s);
     if (!rc) rc = s4_to_e4m3(Wq, N, K, K / 2, B8, K, dev, s);
@@ -259,14 +427,11 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
         M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), SXt);
     k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
         N, Np, nblk, reinterpret_cast<const __half*>(Wscale), SWt);
-    if (rank)
-        k_transpose_v<<<conv_grid(dev, N * rank), 256, 0, s>>>(
-            static_cast<int>(N), static_cast<int>(rank), reinterpret_cast<const __half*>(V), Vt);
     rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
 
     using Cfg = W4A4Cfg;
-    CUtensorMap tA, tB, tXU, tVt, tSX, tSW;
+    CUtensorMap tA, tB, tXU, tV, tSX, tSW;
     rc = make_tmap_kmajor(&tA, false, A8, K, M, K, Cfg::BK, Cfg::BM);
     if (!rc) rc = make_tmap_kmajor(&tB, false, B8, K, N, K, Cfg::BK, Cfg::BN);
     if (!rc) rc = make_tmap_2d(&tSX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SXt, Mp, nblk + 1, Mp * 4,
@@ -276,10 +441,10 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     if (rank) {
         // 32 low-rank columns in a 64-wide (128-byte) box: TMA zero-fills the rest
         if (!rc) rc = make_tmap_kmajor(&tXU, true, XU, rank, M, rank * 2, 64, Cfg::BM);
-        if (!rc) rc = make_tmap_kmajor(&tVt, true, Vt, rank, N, rank * 2, 64, Cfg::BN);
+        if (!rc) rc = make_tmap_kmajor(&tV, true, V, rank, N, rank * 2, 64, Cfg::BN);
     } else {
         tXU = tA;  // never read without the low-rank unit
-        tVt = tB;
+        tV = tB;
     }
     if (rc) return rc;
 
@@ -310,7 +475,7 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     void *pb = nullptr, *pa = nullptr;
     profile_events(&pb, &pa);
     if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), s) != cudaSuccess) return QG_ERR_CUDA;
-    w4a4_gemm_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tA, tB, tXU, tVt, tSX, tSW, p);
+    w4a4_gemm_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tA, tB, tXU, tV, tSX, tSW, p);
     rc = map_cuda(cudaGetLastError());
     if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), s) != cudaSuccess)
         return QG_ERR_CUDA;

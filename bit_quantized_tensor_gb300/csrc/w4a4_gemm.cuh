@@ -107,7 +107,7 @@ enum W4A4Site : int {
 
 __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
     w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmXU, const __grid_constant__ CUtensorMap tmVt,
+                     const __grid_constant__ CUtensorMap tmXU, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmSX, const __grid_constant__ CUtensorMap tmSW,
                      const W4A4Params p) {
     using Cfg = W4A4Cfg;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                         tma_load_2d(db, &tmB, ks * Cfg::BK, nb * Cfg::BN, full_bar(ps.index), pol);
                     } else {
                         tma_load_2d(da, &tmXU, 0, mb * Cfg::BM, full_bar(ps.index), pol);
-                        tma_load_2d(db, &tmVt, 0, nb * Cfg::BN, full_bar(ps.index), pol);
+                        tma_load_2d(db, &tmV, 0, nb * Cfg::BN, full_bar(ps.index), pol);
                     }
                     armed |= 1u << ps.index;
                     armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);

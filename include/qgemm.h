@@ -193,9 +193,11 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K,
  *    s = fp16(max|x| / 7)           (binary32 division, round to nearest even)
  *    q = s == 0 ? 0 : clamp(rint(x / s), -8, 7)   (binary32 division by the
  *        rounded scale, rint round-half-even)
- *  and XU = X . U rounded to fp16 (fp32 accumulation).
+ *  and XU = X . U rounded to fp16 (fp32 accumulation); U is the K x rank
+ *  down-projection L1 of the low-rank branch.
  *  X      : fp32, M x K row-major, ldx >= K.
- *  U      : fp16, K x rank row-major (may be NULL when rank == 0).
+ *  U      : fp16, U transposed: rank x K row-major, the layout of the weight
+ *           of a K -> rank linear layer (may be NULL when rank == 0).
  *  Xq     : s4p output, M x K values, contiguous (M rows of K/2 bytes).
  *  Xscale : fp16 output, M x (K/block), contiguous.
  *  XU     : fp16 output, M x rank, contiguous (ignored when rank == 0).
@@ -212,11 +214,14 @@ int w4a4_quantize(int64_t M, int64_t K, const float *X, int64_t ldx,
  * applied inside the K-sum:
  *  Y[m][n] = sum_j Xscale[m][j]*Wscale[n][j] * sum_{k in block j} Xq[m][k]*Wq[n][k]
  *          + sum_r XU[m][r] * V[r][n] + bias[n],
- *  fp32 accumulation, fp16 result.
+ *  fp32 accumulation, fp16 result; V is the rank x N up-projection L2 of the
+ *  low-rank branch.
  *  Xq, Xscale : as produced by w4a4_quantize (M rows).
  *  Wq, Wscale : the same format for W (N rows).
- *  XU : fp16 M x rank, V : fp16 rank x N row-major, rank 0 or 32 (XU and V
- *       may be NULL when rank == 0).  bias : fp16 N, or NULL.
+ *  XU : fp16 M x rank.  V : fp16, V transposed: N x rank row-major, the
+ *       layout of the weight of a rank -> N linear layer, 16-byte aligned.
+ *       rank 0 or 32 (XU and V may be NULL when rank == 0).
+ *  bias : fp16 N, or NULL.
  *  block : 64.  K multiple of 64.  Y : fp16 M x N row-major, ldy >= N.
  *  ws : workspace of qg_workspace_size(QG_OP_W4A4, M, N, K) bytes, 256-byte
  *       aligned. */

@@ -36,7 +36,7 @@ def _t(a, dev):
 
 def _quant(dev, X, U=None):
     import bit_quantized_tensor_gb300 as qg
-    q, s, xu = qg.w4a4_quantize(_t(X, dev), None if U is None else _t(U, dev), BLOCK)
+    q, s, xu = qg.w4a4_quantize(_t(X, dev), None if U is None else _t(U.T, dev), BLOCK)
     return (q.cpu().numpy(), s.cpu().numpy().view(np.uint16),
             None if xu is None else xu.cpu().numpy())
 
@@ -67,6 +67,38 @@ def test_quantize_golden_edge_cases(dev, oracle):
         vals = oracle.s4_unpack(q[r:r + 1], BLOCK)[0]
         for i, _, qi in c["entries"]:
             assert vals[i] == qi, (c["name"], i)
+
+
+def _near_tie_blocks(M, K, seed):
+    """Blocks whose values sit a few ulps either side of (k + 1/2) * s.
+
+    Each block's first value is 7 * s0 for an fp16 value s0, so the block
+    scale is exactly s0; every other value is (k + 1/2) * s0, exact in fp32,
+    moved by -6..6 ulps.  x / s then lands within a few ulps of a rounding
+    tie, on either side of it or on it.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    nb = K // BLOCK
+    s0 = rng.uniform(-14.0, 3.0, size=(M, nb))
+    s0 = (2.0 ** s0).astype(np.float16).astype(np.float32)
+    s0[:, 0] = np.float32(np.float16(2.0 ** -23))       # fp16-subnormal scales
+    s0[:, 1] = np.float32(np.float16(0.3))              # 1 / s inexact
+    h = rng.integers(-7, 7, size=(M, K)).astype(np.float32) + np.float32(0.5)
+    base = (h * np.repeat(s0, BLOCK, axis=1)).astype(np.float32)
+    d = rng.integers(-6, 7, size=(M, K)).astype(np.int32)
+    mag = (np.abs(base).view(np.int32) + d).view(np.float32)
+    X = np.where(base < 0, -mag, mag).astype(np.float32)
+    X[:, ::BLOCK] = 7.0 * s0
+    return X
+
+
+def test_quantize_near_ties_bit_exact(dev, oracle):
+    M, K = 48, 2048
+    X = _near_tie_blocks(M, K, 91)
+    q, s, _ = _quant(dev, X)
+    q_ref, s_ref = oracle.w4a4_quantize(X, BLOCK)
+    assert np.array_equal(s, s_ref)
+    assert np.array_equal(q, q_ref)
 
 
 def test_quantize_scaled_ranges_bit_exact(dev, oracle):
@@ -125,7 +157,7 @@ def test_gemm_matches_oracle(dev, oracle, M, N, K, rank, bias):
     xu16 = oracle.lowrank_xu(X, U).astype(np.float16) if rank else None
     Y = qg.w4a4_gemm(_t(qx, dev), _t(sx.view(np.float16), dev), _t(qw, dev),
                      _t(sw.view(np.float16), dev), K,
-                     XU=_t(xu16, dev) if rank else None, V=_t(V, dev) if rank else None,
+                     XU=_t(xu16, dev) if rank else None, Vt=_t(V.T, dev) if rank else None,
                      bias=_t(b, dev) if bias else None).cpu().numpy()
     ref = oracle.w4a4_gemm(qx, sx, qw, sw, BLOCK, K,
                            XU=xu16.astype(np.float64) if rank else None,
@@ -153,9 +185,9 @@ def test_end_to_end_full_size_sampled(dev, oracle):
     M, N, K = 4096, 8192, 8192
     X, W, U, V, b = _gemm_case(M, N, K, 4)
     tX, tW = _t(X, dev), _t(W, dev)
-    qx, sx, xu = qg.w4a4_quantize(tX, _t(U, dev), BLOCK)
+    qx, sx, xu = qg.w4a4_quantize(tX, _t(U.T, dev), BLOCK)
     qw, sw, _ = qg.w4a4_quantize(tW, None, BLOCK)
-    Y = qg.w4a4_gemm(qx, sx, qw, sw, K, XU=xu, V=_t(V, dev), bias=_t(b, dev)).cpu().numpy()
+    Y = qg.w4a4_gemm(qx, sx, qw, sw, K, XU=xu, Vt=_t(V.T, dev), bias=_t(b, dev)).cpu().numpy()
     rows = inputs.sample_rows(M, 24, 5104)
     qx_r, sx_r = oracle.w4a4_quantize(X[rows], BLOCK)
     qw_r, sw_r = oracle.w4a4_quantize(W, BLOCK)
