@@ -175,6 +175,8 @@ static int launch_tc2(const void* A, int64_t lda_bytes, const void* B, int64_t l
 // 1 = always one CTA per tile, 2 = always CTA pairs.  Testing hook.
 static std::atomic<int> g_gemm_path{0};
 
+int gemm_path() { return g_gemm_path.load(); }
+
 static bool use_pairs(int64_t M, int64_t N) {
     const int path = g_gemm_path.load();
     if (path == 1) return false;

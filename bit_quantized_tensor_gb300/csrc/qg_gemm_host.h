@@ -13,6 +13,10 @@ int make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
                  int64_t outer, int64_t row_stride_bytes, int box_inner, int box_outer,
                  CUtensorMapSwizzle swizzle);
 
+// Kernel choice set by qg_set_gemm_path: 0 by shape, 1 one CTA per tile,
+// 2 CTA pairs.
+int gemm_path();
+
 // The caller-owned events of qg_set_profile_events (null when unset).
 void profile_events(void** before, void** after);
 

@@ -17,7 +17,9 @@
 #include <mutex>
 
 #include "qg_gemm_host.h"
+#include "tc_gemm2.cuh"
 #include "w4a4_gemm.cuh"
+#include "w4a4_gemm2.cuh"
 
 namespace qg {
 
@@ -336,6 +338,67 @@ __global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
 
 }  // namespace qg
 
+namespace qg {
+
+// Tensor maps and launch of one of the two W4A4 GEMM kernels (one CTA per
+// 128 x 192 tile, or CTA pairs per 256 x 128 tile).
+template <class Cfg, bool PAIR>
+static int launch_w4a4(const uint8_t* A8, const uint8_t* B8, const float* SXt, const float* SWt,
+                       const uint16_t* XU, const uint16_t* V, int64_t M, int64_t N, int64_t K,
+                       int64_t Mp, int64_t Np, int64_t rank, const W4A4Params& p, int dev,
+                       cudaStream_t s) {
+    constexpr int B_ROWS = PAIR ? Cfg::BN / 2 : Cfg::BN;
+    const int nblk = p.nblk;
+    CUtensorMap tA, tB, tXU, tV, tSX, tSW;
+    int rc = make_tmap_kmajor(&tA, false, A8, K, M, K, Cfg::BK, Cfg::BM);
+    if (!rc) rc = make_tmap_kmajor(&tB, false, B8, K, N, K, Cfg::BK, B_ROWS);
+    if (!rc) rc = make_tmap_2d(&tSX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SXt, Mp, nblk + 1, Mp * 4,
+                               Cfg::BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!rc) rc = make_tmap_2d(&tSW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SWt, Np, nblk + 1, Np * 4,
+                               Cfg::BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rank) {
+        // 32 low-rank columns in a 64-wide (128-byte) box: TMA zero-fills the rest
+        if (!rc) rc = make_tmap_kmajor(&tXU, true, XU, rank, M, rank * 2, 64, Cfg::BM);
+        if (!rc) rc = make_tmap_kmajor(&tV, true, V, rank, N, rank * 2, 64, B_ROWS);
+    } else {
+        tXU = tA;  // never read without the low-rank unit
+        tV = tB;
+    }
+    if (rc) return rc;
+
+    auto kernel = PAIR ? w4a4_gemm2_kernel : w4a4_gemm_kernel;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    int grid;
+    if (PAIR) {
+        const int64_t tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
+        const int64_t max_pairs = num_sms(dev) / 2;
+        grid = 2 * static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    } else {
+        const int64_t tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
+        grid = static_cast<int>(tiles < num_sms(dev) ? tiles : num_sms(dev));
+    }
+    void *pb = nullptr, *pa = nullptr;
+    profile_events(&pb, &pa);
+    if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), s) != cudaSuccess) return QG_ERR_CUDA;
+    kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tA, tB, tXU, tV, tSX, tSW, p);
+    rc = map_cuda(cudaGetLastError());
+    if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), s) != cudaSuccess)
+        return QG_ERR_CUDA;
+    return rc;
+}
+
+}  // namespace qg
+
 using namespace qg;
 
 extern "C" {
@@ -430,56 +493,21 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
 
-    using Cfg = W4A4Cfg;
-    CUtensorMap tA, tB, tXU, tV, tSX, tSW;
-    rc = make_tmap_kmajor(&tA, false, A8, K, M, K, Cfg::BK, Cfg::BM);
-    if (!rc) rc = make_tmap_kmajor(&tB, false, B8, K, N, K, Cfg::BK, Cfg::BN);
-    if (!rc) rc = make_tmap_2d(&tSX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SXt, Mp, nblk + 1, Mp * 4,
-                               Cfg::BM, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!rc) rc = make_tmap_2d(&tSW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, SWt, Np, nblk + 1, Np * 4,
-                               Cfg::BN, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (rank) {
-        // 32 low-rank columns in a 64-wide (128-byte) box: TMA zero-fills the rest
-        if (!rc) rc = make_tmap_kmajor(&tXU, true, XU, rank, M, rank * 2, 64, Cfg::BM);
-        if (!rc) rc = make_tmap_kmajor(&tV, true, V, rank, N, rank * 2, 64, Cfg::BN);
-    } else {
-        tXU = tA;  // never read without the low-rank unit
-        tV = tB;
-    }
-    if (rc) return rc;
-
-    static std::mutex mu;
-    static bool attr_set[64] = {};
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (!attr_set[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                w4a4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-            if (e != cudaSuccess) return map_cuda(e);
-            attr_set[dev] = true;
-        }
-    }
     W4A4Params p;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.num_ks = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
+    p.num_ks = static_cast<int>((K + W4A4Cfg::BK - 1) / W4A4Cfg::BK);
     p.nblk = nblk;
     p.lowrank = rank ? 1 : 0;
     p.Y = reinterpret_cast<__half*>(Y);
     p.ldy = ldy;
     p.bias = reinterpret_cast<const __half*>(bias);
     p.ctl = ctl;
-    const int64_t tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
-    const int grid = static_cast<int>(tiles < num_sms(dev) ? tiles : num_sms(dev));
-    void *pb = nullptr, *pa = nullptr;
-    profile_events(&pb, &pa);
-    if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), s) != cudaSuccess) return QG_ERR_CUDA;
-    w4a4_gemm_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(tA, tB, tXU, tV, tSX, tSW, p);
-    rc = map_cuda(cudaGetLastError());
-    if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), s) != cudaSuccess)
-        return QG_ERR_CUDA;
-    return rc;
+    const int path = gemm_path();
+    const bool pairs = path == 2 || (path == 0 && M > W4A4Cfg::BM);
+    return pairs ? launch_w4a4<W4A4PairCfg, true>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s)
+                 : launch_w4a4<W4A4Cfg, false>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s);
 }
 
 }  // extern "C"

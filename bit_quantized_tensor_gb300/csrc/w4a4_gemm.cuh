@@ -9,9 +9,8 @@
 // an exact integer computed by tcgen05 kind::f8f6f4 into its own TMEM
 // buffer.  The epilogue warps apply the two block scales in fp32 and add the
 // result to a register-resident fp32 tile:
-//     t = P_j * sW[n][j]   (exact: 13-bit integer times an fp16 value)
-//     acc = fma(t, sX[m][j], acc)   (one rounding per block)
-// using packed f32x2 arithmetic, two columns per instruction.  The low-rank
+//     c = sW[n][j] * sX[m][j]   (packed f32x2, two columns per instruction)
+//     acc = fma(P_j, c, acc)    (one rounding per block)  The low-rank
 // term XU . V is one more accumulation unit per tile: a kind::f16 MMA over
 // the 32 low-rank columns (TMA zero-fills them to a 64-wide tile), scaled by
 // the constant 1 row appended to the scale tables.  The bias is added before
@@ -30,25 +29,34 @@
 
 namespace qg {
 
-__device__ __forceinline__ void mul_f32x2(float& d0, float& d1, float a0, float a1, float b0,
-                                          float b1) {
-    asm("{\n.reg .b64 a, b, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %5};\n"
-        "mul.rn.f32x2 d, a, b;\nmov.b64 {%0, %1}, d;\n}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+// Packed pairs of fp32 values in one 64-bit register (low half = first).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
 }
-
-__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0,
-                                          float b1) {
-    asm("{\n.reg .b64 a, b, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %5};\n"
-        "mov.b64 d, {%0, %1};\nfma.rn.f32x2 d, a, b, d;\nmov.b64 {%0, %1}, d;\n}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
 struct W4A4Cfg {
-    // N = 192 lets 12 epilogue warps (3 per TMEM lane quadrant, 64 columns
-    // each) hold their fp32 accumulators in registers within a 14-warp block.
+    // N = 192 lets 16 epilogue warps (4 per TMEM lane quadrant, 48 columns
+    // each) hold their fp32 accumulators in registers within an 18-warp block.
     static constexpr int BM = 128, BN = 192;
     static constexpr int ROW_BYTES = 128;                 // 128 e4m3 per stage row = 2 blocks
     static constexpr int BK = 128;
@@ -68,8 +76,8 @@ struct W4A4Cfg {
     static constexpr int SMEM_LIMIT = 232448;
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EPI_WARPS = 12;
-    static constexpr int EPI_COLS = BN / 3;               // columns per epilogue warp
+    static constexpr int EPI_WARPS = 16;
+    static constexpr int EPI_COLS = BN / 4;               // columns per epilogue warp
     static constexpr int THREADS = 32 * (2 + EPI_WARPS);
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * SC_STAGES + 2 * ACC_BUFS + 1;
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, BM, BN);  // e4m3 or f16 x2, f32 acc
@@ -80,7 +88,7 @@ struct W4A4Cfg {
     static_assert(ACC_BUFS * BN <= TMEM_COLS, "TMEM budget exceeded");
     static_assert(SC_BYTES % 128 == 0 && STAGE_BYTES % 1024 == 0, "alignment of ring slots");
     static_assert(EPI_COLS % 16 == 0 && BN % 16 == 0 && BN <= 256, "epilogue column split");
-    static_assert(THREADS <= 512, "more than 16 warps would cap registers at 96");
+    static_assert(THREADS <= 576, "more than 18 warps would cap registers below 112");
 };
 
 struct W4A4Params {
@@ -279,20 +287,31 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
+        // Warp (quad, colpart) owns TMEM lanes [32 quad, 32 quad + 32) and
+        // columns [48 colpart, 48 colpart + 48) of the tile, read as two
+        // 16-lane halves in the m16n8-accumulator layout: lane (g, q) holds
+        // rows 32 quad + 16 hf + g (+ 8) and columns 8c + 2q (+ 1) for the
+        // six column groups c, so per block it needs 4 row scales and 6
+        // column-scale pairs, all from distinct shared-memory words.  The
+        // three 16-column chunks are loaded one ahead of the arithmetic.
+        constexpr int NCH = Cfg::EPI_COLS / 16;
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const int colpart = (warp - 2) >> 2;     // which third of the tile's columns
+        const int colpart = (warp - 2) >> 2;     // which quarter of the tile's columns
+        const int g = lane >> 2, q = lane & 3;
         PipeState<ACC> as;
         PipeState<SCS> ss;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
             int mb, nb;
             tile_coords(t, num_m, num_n, mb, nb);
-            const int rloc = quad * 32 + lane;
-            const int row = mb * Cfg::BM + rloc;
-            const int col0 = nb * Cfg::BN + colpart * Cfg::EPI_COLS;
-            float acc[Cfg::EPI_COLS];
+            // acc[hf][c][2e + d]: row 16 hf + g + 8e, column 8c + 2q + d
+            float acc[2][2 * NCH][4];
 #pragma unroll
-            for (int i = 0; i < Cfg::EPI_COLS; ++i) acc[i] = 0.f;
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int c = 0; c < 2 * NCH; ++c)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[hf][c][i] = 0.f;
             const int steps = p.num_ks + p.lowrank;
             for (int ks = 0; ok && ks < steps; ++ks) {
                 const int units = (ks == p.num_ks) ? 1 : 2;
@@ -312,27 +331,46 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const float sx = sx_s[h * Cfg::BM + rloc];
-                    const float* swc = sw_s + h * Cfg::BN + colpart * Cfg::EPI_COLS;
+                    const float* sxr = sx_s + h * Cfg::BM + quad * 32 + g;
+                    const float* swc = sw_s + h * Cfg::BN + colpart * Cfg::EPI_COLS + 2 * q;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                            static_cast<uint32_t>(as.index * Cfg::BN +
                                                                  colpart * Cfg::EPI_COLS);
+                    uint32_t rb[2][2][8];  // [buffer][half][x2 registers]
 #pragma unroll
-                    for (int c = 0; c < Cfg::EPI_COLS / 16; ++c) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(taddr + 16u * c, r);
-                        tmem_wait_ld();
+                    for (int hf = 0; hf < 2; ++hf)
+                        tmem_ld_16x256b_x2(taddr + (static_cast<uint32_t>(16 * hf) << 16), rb[0][hf]);
+                    // row-scale pairs (s, s) for rows g, g + 8, 16 + g, 24 + g
+                    uint64_t sxp[4];
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4) {
-                            const float4 w = *reinterpret_cast<const float4*>(swc + 16 * c + i);
-                            float t0, t1, t2, t3;
-                            mul_f32x2(t0, t1, __uint_as_float(r[i]), __uint_as_float(r[i + 1]), w.x,
-                                      w.y);
-                            mul_f32x2(t2, t3, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]),
-                                      w.z, w.w);
-                            fma_f32x2(acc[16 * c + i], acc[16 * c + i + 1], t0, t1, sx, sx);
-                            fma_f32x2(acc[16 * c + i + 2], acc[16 * c + i + 3], t2, t3, sx, sx);
+                    for (int k = 0; k < 4; ++k) sxp[k] = pack_f32x2(sxr[8 * k], sxr[8 * k]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        if (ch + 1 < NCH) {
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf)
+                                tmem_ld_16x256b_x2(taddr + (static_cast<uint32_t>(16 * hf) << 16) +
+                                                       static_cast<uint32_t>(16 * (ch + 1)),
+                                                   rb[(ch + 1) & 1][hf]);
                         }
+                        // c = sW * sX for the chunk's 2 column pairs and 4 rows, as
+                        // packed pairs (both factors already paired in registers)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const uint64_t w = *reinterpret_cast<const uint64_t*>(swc + 16 * ch + 8 * i);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const float2 c = unpack_f32x2(mul2(w, sxp[2 * hf + e]));
+                                    const uint32_t* r = &rb[ch & 1][hf][4 * i + 2 * e];
+                                    float* a = &acc[hf][2 * ch + i][2 * e];
+                                    a[0] = __fmaf_rn(__uint_as_float(r[0]), c.x, a[0]);
+                                    a[1] = __fmaf_rn(__uint_as_float(r[1]), c.y, a[1]);
+                                }
+                        }
+                        if (ch + 1 < NCH) tmem_wait_ld();
                     }
                     tc_fence_before();
                     __syncwarp();
@@ -345,9 +383,32 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                 ss.advance();
             }
             if (!ok) break;
-            if (row < p.M)
-                store_row_f16<Cfg::EPI_COLS>(p.Y + static_cast<int64_t>(row) * p.ldy + col0, col0, p.N,
-                                             acc, p.bias);
+            // fp16 store (+ bias): per row pairs of adjacent columns
+            const int colb = nb * Cfg::BN + colpart * Cfg::EPI_COLS + 2 * q;
+            const bool pair_ok = (p.ldy & 1) == 0;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = mb * Cfg::BM + quad * 32 + 16 * hf + 8 * e + g;
+                    if (row >= p.M) continue;
+                    __half* yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
+#pragma unroll
+                    for (int c = 0; c < 2 * NCH; ++c) {
+                        const int col = colb + 8 * c;
+                        float v0 = acc[hf][c][2 * e], v1 = acc[hf][c][2 * e + 1];
+                        if (p.bias) {
+                            if (col < p.N) v0 += __half2float(p.bias[col]);
+                            if (col + 1 < p.N) v1 += __half2float(p.bias[col + 1]);
+                        }
+                        if (pair_ok && col + 1 < p.N) {
+                            *reinterpret_cast<__half2*>(yrow + col) = __floats2half2_rn(v0, v1);
+                        } else {
+                            if (col < p.N) yrow[col] = __float2half_rn(v0);
+                            if (col + 1 < p.N) yrow[col + 1] = __float2half_rn(v1);
+                        }
+                    }
+                }
         }
     }
 

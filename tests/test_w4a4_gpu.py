@@ -146,11 +146,25 @@ def _gemm_case(M, N, K, seed, rank=RANK, with_bias=True):
     return X, W, U, V, b
 
 
-@pytest.mark.parametrize("M,N,K,rank,bias", [(1, 8, 64, 32, True), (100, 300, 256, 32, True),
-                                             (129, 257, 576, 32, False), (64, 512, 1024, 0, True),
-                                             (256, 256, 4096, 0, False)])
-def test_gemm_matches_oracle(dev, oracle, M, N, K, rank, bias):
+@pytest.fixture
+def gemm_path():
     import bit_quantized_tensor_gb300 as qg
+    def set_path(p):
+        assert qg.lib().qg_set_gemm_path(p) == 0
+    yield set_path
+    qg.lib().qg_set_gemm_path(0)
+
+
+GEMM_SHAPES = [(1, 8, 64, 32, True), (100, 300, 256, 32, True), (129, 257, 576, 32, False),
+               (64, 512, 1024, 0, True), (256, 256, 4096, 0, False), (300, 136, 192, 32, True),
+               (520, 392, 1088, 32, True)]
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K,rank,bias", GEMM_SHAPES)
+def test_gemm_matches_oracle(dev, oracle, gemm_path, path, M, N, K, rank, bias):
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
     X, W, U, V, b = _gemm_case(M, N, K, 7, rank, bias)
     qx, sx = oracle.w4a4_quantize(X, BLOCK)
     qw, sw = oracle.w4a4_quantize(W, BLOCK)
@@ -165,10 +179,12 @@ def test_gemm_matches_oracle(dev, oracle, M, N, K, rank, bias):
     assert_fp16_close(Y, ref, f"w4a4 {M}x{N}x{K} r={rank}")
 
 
-def test_gemm_unit_scales_equal_int4_gemm(dev, oracle):
+@pytest.mark.parametrize("path", [1, 2])
+def test_gemm_unit_scales_equal_int4_gemm(dev, oracle, gemm_path, path):
     # sX = sW = 1 and no low-rank term: Y is the INT4 GEMM rounded to fp16
     # (exact while |Y| <= 2048)
     import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
     M, N, K = 96, 160, 64
     qx = inputs.s4_packed_uniform(M, K, 21)
     qw = inputs.s4_packed_uniform(N, K, 22)
