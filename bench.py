@@ -42,6 +42,10 @@ FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Nominal dense tensor rates relative to bf16/fp16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5.
 FP8_RATIO, FP4_RATIO = 2.0, 6.0
+# DRAM bytes (read + write) of one qgemm_s8 main-kernel launch at 8192^3, from
+# Nsight Compute (dram__bytes_read.sum + dram__bytes_write.sum); None until
+# measured for the current kernel (the capture command is in the profiles).
+S8_MAIN_DRAM_BYTES = 1086626560 + 250137600
 
 
 def load_peaks():
@@ -337,10 +341,13 @@ def run_ours(args, rank, world, local_rank):
     }
     k_ms = medk["s8"]
     achieved = tops(gemm_ops, k_ms)
-    roofline = {"bound": "tensor", "kernel": "tc_gemm_kernel<F16,S32> (qgemm_s8 main GEMM)",
+    roofline = {"bound": "tensor",
+                "kernel": "tc_gemm2_kernel<Tc2Cfg<F16,S32>> (qgemm_s8 main GEMM, CTA pairs)",
                 "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 dense (fp16 kind runs at the bf16 rate)",
-                "frac": round(achieved / bf16, 3), "traffic": None}
+                "frac": round(achieved / bf16, 3), "traffic": S8_MAIN_DRAM_BYTES,
+                "traffic_unit": "bytes per launch (DRAM read + write, one Nsight Compute capture)",
+                "algorithmic_bytes": 2 * 2 * N_SQ * N_SQ + 4 * N_SQ * N_SQ}
 
     result = {
         "metric": METRIC, "value": round(s8_tops, 1), "unit": "TOPS", "n_gpus": world,

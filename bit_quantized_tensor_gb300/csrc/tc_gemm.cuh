@@ -95,15 +95,18 @@ struct TcGemmParams {
     Ctl ctl;
 };
 
-// Tiles are visited in groups of kGroupM row-blocks so that the CTAs running
-// at the same time share A and B tiles in L2.
+// Tiles are visited in groups of `group_m` row-blocks (column-major inside a
+// group) so that the CTAs running at the same time cover a compact block of
+// the output and share their A and B tiles through L2: one CTA per SM covers
+// 16 row-blocks x ~10 column-blocks, CTA pairs 8 x ~10.
 constexpr int kGroupM = 16;
-
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
-    const int group_size = kGroupM * num_n;
+constexpr int kGroupMPairs = 8;
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb,
+                                            int group_m = kGroupM) {
+    const int group_size = group_m * num_n;
     const int g = t / group_size;
-    const int first_m = g * kGroupM;
-    const int gm = min(kGroupM, num_m - first_m);
+    const int first_m = g * group_m;
+    const int gm = min(group_m, num_m - first_m);
     const int local = t - g * group_size;
     mb = first_m + local % gm;
     nb = local / gm;

@@ -132,7 +132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             bool ok = true;
             for (int t = pair; ok && t < ntiles; t += npairs) {
                 int mb, nb;
-                tile_coords(t, num_m, num_n, mb, nb);
+                tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
                 const int arow = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM;
                 const int brow = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -220,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         bool ok = true;
         for (int t = pair; ok && t < ntiles; t += npairs) {
             int mb, nb;
-            tile_coords(t, num_m, num_n, mb, nb);
+            tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
             const int row = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM + quad * 32 + lane;
             const int col0 = nb * Cfg::BN + colhalf * 128;
             if constexpr (Cfg::EPI == Epi::S32) {

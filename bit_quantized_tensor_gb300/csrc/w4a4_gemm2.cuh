@@ -156,7 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
             bool ok = true;
             for (int t = pair; ok && t < ntiles; t += npairs) {
                 int mb, nb;
-                tile_coords(t, num_m, num_n, mb, nb);
+                tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
                 const int arow = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM;
                 const int brow = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 for (int ks = 0; ks < steps; ++ks) {
@@ -289,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
         bool ok = true;
         for (int t = pair; ok && t < ntiles; t += npairs) {
             int mb, nb;
-            tile_coords(t, num_m, num_n, mb, nb);
+            tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
             // acc[hf][c][2e + d]: row 16 hf + g + 8e, column 8c + 2q + d
             float acc[2][NG][4];
 #pragma unroll
