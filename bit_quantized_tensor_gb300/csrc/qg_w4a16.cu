@@ -216,31 +216,35 @@ __global__ void __launch_bounds__(kW16Threads)
 //
 // In a chain of layers a call can only use X once the previous call has
 // finished, so everything that does not need X comes first:
-//  - at entry one thread bulk-copies the CTA's 16 weight rows into shared
-//    memory (cp.async.bulk: a few large transfers, the whole slab in flight
-//    at once), before the previous kernel has finished;
-//  - after griddepcontrol.wait each warp stages only its own K slice of X,
-//    already regrouped into the pair order the MMA fragments use, so the
-//    inner loop reads a fragment with one 16-byte shared load.
-// The per-weight work is the dequantization, exact in fp16: one lop3 per
-// fp16 pair does the two's-complement fix (XOR 8), the mask and the exponent
-// OR at once; even k gives 1024 + (v + 8) (minus 1032 -> v), odd k gives
-// 1024 + 16 (v + 8) (times 1/16 minus 72 -> v).  Group scales are applied
-// in fp32 after each group's MMAs.  CTA: one 16-row weight tile, 8 warps,
-// warp w on K slice w; partial tiles are added through shared memory.
-constexpr int kXRowPad = 32;
+//  - at entry 16 lanes bulk-copy the CTA's 16 weight rows into shared memory
+//    (cp.async.bulk, the whole slab in flight at once) and the CTA copies the
+//    rows' group scales next to them, before the previous kernel has
+//    finished;
+//  - after griddepcontrol.wait each warp loads the X values of its own K
+//    slice straight into MMA fragment registers.
+// The arithmetic after the wait is spread over 16 warps (warp w on K slice
+// w) so that the part of a call that cannot overlap the previous one stays
+// short.  The per-weight work is the dequantization, exact in fp16: one lop3
+// per fp16 pair does the two's-complement fix (XOR 8), the mask and the
+// exponent OR at once; even k gives 1024 + (v + 8) (minus 1032 -> v), odd k
+// gives 1024 + 16 (v + 8) (times 1/16 minus 72 -> v).  Group scales are
+// applied in fp32 after each group's MMAs; the 16 slices' partial tiles are
+// added through shared memory.
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = 32 * kDecWarps;
 constexpr int kWRowPad = 64;
-constexpr size_t kDecMaxSmem = 200 * 1024;  // dynamic shared memory for weights + X
+constexpr size_t kDecMaxSmem = 200 * 1024;  // dynamic shared memory
 constexpr int kSiteW16Bulk = 301;
 constexpr int kSiteW16Drain = 302;
 
-__device__ __forceinline__ int xs_swizzle(int chunk) { return chunk ^ ((chunk >> 3) & 1); }
-
-// Weights: 16 rows of K/2 bytes (+ pad).  X: 8 warp slices of M rows, each
-// ceil(G/8) groups of 128 halves (+ pad).
+// Shared memory of one CTA: 16 weight rows of K/2 bytes (+ pad), the rows'
+// group scales (16 x (G + 2) halves: the odd word stride spreads the rows over
+// the banks), and the partial tiles of the 16 warps.
+__host__ __device__ constexpr size_t dec_w_bytes(int64_t K) { return 16 * static_cast<size_t>(K / 2 + kWRowPad); }
+__host__ __device__ constexpr size_t dec_s_stride(int64_t K) { return static_cast<size_t>(K / 128 + 2); }
 __host__ __device__ constexpr size_t dec_smem_bytes(int64_t M, int64_t K) {
-    return 16 * static_cast<size_t>(K / 2 + kWRowPad) +
-           8 * static_cast<size_t>(M) * (256 * static_cast<size_t>((K / 128 + 7) / 8) + kXRowPad);
+    return dec_w_bytes(K) + ((16 * dec_s_stride(K) * 2 + 15) / 16) * 16 +
+           static_cast<size_t>(kDecWarps) * (M <= 8 ? 1 : 2) * 4 * 32 * 4;
 }
 
 // d = b ? (c ? ~a : a) : c, bitwise: with b = mask and c = (exponent bits
@@ -273,26 +277,33 @@ __device__ __forceinline__ void dequant_word_fast(uint32_t w, uint32_t (&p)[4]) 
     p[3] = *reinterpret_cast<uint32_t*>(&v3);
 }
 
+// X fragment of 8 consecutive k (one 16-byte load) in the pair order of
+// dequant_word_fast: (x0, x4), (x1, x5), (x2, x6), (x3, x7).
+__device__ __forceinline__ uint4 x_pairs(uint4 v) {
+    return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                      __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+}
+
 template <int MB>  // batch tiles of 8 rows: M <= 8 * MB
-__global__ void __launch_bounds__(kW16Threads, 2)
+__global__ void __launch_bounds__(kDecThreads, 2)
     k_w4a16_dec(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
                 const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
                 int64_t ldy, const Ctl ctl) {
     extern __shared__ __align__(16) uint8_t dsm[];
-    __shared__ float red[8][MB * 4][32];
     __shared__ __align__(8) uint64_t wbar;
     __shared__ int failed;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int G = K / kGroup;
-    const int gpw = (G + 7) / 8;
+    const int gpw = (G + kDecWarps - 1) / kDecWarps;
     const int gbeg = min(G, warp * gpw), gend = min(G, gbeg + gpw);
     const int n0 = blockIdx.x * 16;
     const int rows = min(16, N - n0);
-    const int wrs = K / 2 + kWRowPad;          // bytes per staged weight row
-    const int xrs = 256 * gpw + kXRowPad;      // bytes per staged X row of one warp's slice
+    const int wrs = K / 2 + kWRowPad;                           // bytes per staged weight row
+    const int sst = static_cast<int>(dec_s_stride(K));          // halves per staged scale row
     uint8_t* ws = dsm;
-    uint8_t* xw = dsm + 16 * wrs + warp * M * xrs;  // this warp's X slice
+    unsigned short* ss = reinterpret_cast<unsigned short*>(dsm + dec_w_bytes(K));
+    float* red = reinterpret_cast<float*>(dsm + dec_w_bytes(K) + ((16 * sst * 2 + 15) / 16) * 16);
     const uint32_t bar = smem_u32(&wbar);
 
     if (threadIdx.x == 0) {
@@ -310,32 +321,15 @@ __global__ void __launch_bounds__(kW16Threads, 2)
                           static_cast<uint32_t>(K / 2), bar);
     }
     pdl_launch_dependents();
-
-    // Scales stay raw 16-bit until used.
-    unsigned short s0[8], s1[8];
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const int gi = gbeg + b;
-        s0[b] = (gi < gend && g < rows) ? ld_nc_u16(S + static_cast<int64_t>(n0 + g) * G + gi) : 0;
-        s1[b] = (gi < gend && g + 8 < rows) ? ld_nc_u16(S + static_cast<int64_t>(n0 + g + 8) * G + gi)
-                                            : 0;
+    // group scales of the 16 rows (raw 16-bit; rows past N read as 0)
+    for (int i = threadIdx.x; i < 16 * G; i += kDecThreads) {
+        const int r = i / G, gi = i - r * G;
+        ss[r * sst + gi] = r < rows ? ld_nc_u16(S + static_cast<int64_t>(n0 + r) * G + gi) : 0;
     }
+    __syncthreads();  // scales staged
 
-    // X may be the previous kernel's output: stage this warp's slice only now,
-    // each 8-k chunk as the pairs (x0,x4), (x1,x5), (x2,x6), (x3,x7).
+    // X may be the previous kernel's output: read it only now.
     pdl_wait_prior_grid();
-    {
-        const int kbase = gbeg * kGroup;
-        const int cpr = (gend - gbeg) * (kGroup / 8);  // 16-byte chunks per row of the slice
-        for (int c = lane; c < M * cpr; c += 32) {
-            const int r = c / cpr, cc = c - r * cpr;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + r * ldx + kbase + cc * 8));
-            const uint4 o = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                                       __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
-            *reinterpret_cast<uint4*>(xw + r * xrs + xs_swizzle(cc) * 16) = o;
-        }
-        __syncwarp();
-    }
     if (!bounded_wait(bar, 0u, nullptr, ctl, kSiteW16Bulk)) {
         failed = 1;
         if (lane == 0) bounded_wait(bar, 0u, nullptr, ctl, kSiteW16Drain);
@@ -347,56 +341,58 @@ __global__ void __launch_bounds__(kW16Threads, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mb][i] = 0.f;
 
-    for (int gb = gbeg; gb < gend; gb += 8) {
+    for (int gi = gbeg; gi < gend; ++gi) {
+        // X fragments of this group: lane (g, t) holds batch row mb*8 + g at
+        // k = 32t + 8i + 0..7, i = 0..3
+        uint4 xf[MB][4];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int gi = gb + b;
-            if (gi >= gend) break;
-            uint4 w0 = make_uint4(0u, 0u, 0u, 0u);  // nibbles 0: rows past N contribute 0
-            uint4 w1 = w0;
-            if (g < rows) w0 = *reinterpret_cast<const uint4*>(ws + g * wrs + gi * 64 + 16 * t);
-            if (g + 8 < rows)
-                w1 = *reinterpret_cast<const uint4*>(ws + (g + 8) * wrs + gi * 64 + 16 * t);
-            float tmp[MB][4];
+        for (int mb = 0; mb < MB; ++mb) {
+            const int m = mb * 8 + g;
 #pragma unroll
-            for (int mb = 0; mb < MB; ++mb)
+            for (int i = 0; i < 4; ++i)
+                xf[mb][i] = m < M ? x_pairs(__ldg(reinterpret_cast<const uint4*>(
+                                        X + static_cast<int64_t>(m) * ldx + gi * kGroup + 32 * t + 8 * i)))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        }
+        uint4 w0 = make_uint4(0u, 0u, 0u, 0u);  // nibbles 0: rows past N contribute 0
+        uint4 w1 = w0;
+        if (g < rows) w0 = *reinterpret_cast<const uint4*>(ws + g * wrs + gi * 64 + 16 * t);
+        if (g + 8 < rows) w1 = *reinterpret_cast<const uint4*>(ws + (g + 8) * wrs + gi * 64 + 16 * t);
+        float tmp[MB][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) tmp[mb][i] = 0.f;
-            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-            const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
+        for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t pa[4], pb[4];
-                dequant_word_fast(wa[i], pa);
-                dequant_word_fast(wb[i], pb);
-                const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
-                const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
-                const int chunk = ((gi - gbeg) * kGroup + 32 * t + 8 * i) >> 3;
+            for (int i = 0; i < 4; ++i) tmp[mb][i] = 0.f;
+        const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+        const uint32_t wb[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                for (int mb = 0; mb < MB; ++mb) {
-                    const int m = mb * 8 + g;
-                    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-                    if (m < M) xv = *reinterpret_cast<const uint4*>(xw + m * xrs + xs_swizzle(chunk) * 16);
-                    mma_16816(tmp[mb], a0, xv.x, xv.y);
-                    mma_16816(tmp[mb], a1, xv.z, xv.w);
-                }
-            }
-            const float sc0 = __half2float(__ushort_as_half(s0[(gi - gbeg) & 7]));
-            const float sc1 = __half2float(__ushort_as_half(s1[(gi - gbeg) & 7]));
+        for (int i = 0; i < 4; ++i) {
+            uint32_t pa[4], pb[4];
+            dequant_word_fast(wa[i], pa);
+            dequant_word_fast(wb[i], pb);
+            const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+            const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
-                acc[mb][0] = fmaf(tmp[mb][0], sc0, acc[mb][0]);
-                acc[mb][1] = fmaf(tmp[mb][1], sc0, acc[mb][1]);
-                acc[mb][2] = fmaf(tmp[mb][2], sc1, acc[mb][2]);
-                acc[mb][3] = fmaf(tmp[mb][3], sc1, acc[mb][3]);
+                mma_16816(tmp[mb], a0, xf[mb][i].x, xf[mb][i].y);
+                mma_16816(tmp[mb], a1, xf[mb][i].z, xf[mb][i].w);
             }
+        }
+        const float sc0 = __half2float(__ushort_as_half(ss[g * sst + gi]));
+        const float sc1 = __half2float(__ushort_as_half(ss[(g + 8) * sst + gi]));
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+            acc[mb][0] = fmaf(tmp[mb][0], sc0, acc[mb][0]);
+            acc[mb][1] = fmaf(tmp[mb][1], sc0, acc[mb][1]);
+            acc[mb][2] = fmaf(tmp[mb][2], sc1, acc[mb][2]);
+            acc[mb][3] = fmaf(tmp[mb][3], sc1, acc[mb][3]);
         }
     }
 
 #pragma unroll
     for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) red[warp][mb * 4 + i][lane] = acc[mb][i];
+        for (int i = 0; i < 4; ++i) red[(warp * MB * 4 + mb * 4 + i) * 32 + lane] = acc[mb][i];
     __syncthreads();
     if (warp >= MB || failed) return;
     // warp mb writes batch tile mb: lane (g, t) holds Y[mb*8 + 2t + {0,1}][n0 + g / n0 + g + 8]
@@ -406,7 +402,7 @@ __global__ void __launch_bounds__(kW16Threads, 2)
     for (int i = 0; i < 4; ++i) {
         float sum = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sum += red[q][mb * 4 + i][lane];
+        for (int q = 0; q < kDecWarps; ++q) sum += red[(q * MB * 4 + mb * 4 + i) * 32 + lane];
         v[i] = sum;
     }
 #pragma unroll
@@ -449,7 +445,7 @@ static int launch_w4a16_dec(int M, int N, int K, const __half* X, int64_t ldx, c
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((N + 15) / 16));
-    cfg.blockDim = dim3(kW16Threads);
+    cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

@@ -51,7 +51,9 @@ def test_w4a16_4096(dev, oracle, M):
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 128), (1, 1, 128), (3, 100, 256), (17, 260, 384),
                                    (40, 72, 1024), (77, 333, 640), (130, 48, 256),
-                                   (9, 4096, 11008 // 128 * 128), (2, 64, 8192)])
+                                   (9, 4096, 11008 // 128 * 128), (2, 64, 8192),
+                                   (1, 40, 16384), (12, 40, 20480), (1, 24, 20480),
+                                   (5, 33, 24576)])
 def test_w4a16_shapes(dev, oracle, M, N, K):
     X, Wq, S = _operands(M, N, K, idx=M + N)
     assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), f"w4a16 {M}x{N}x{K}")
