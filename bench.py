@@ -8,7 +8,8 @@ HBM:
   gemm_f16   8192 x 8192 x 8192, N(0,1) fp16 -> fp16 (fp32 accumulation)
   w4a16_gemm M=1, N=K=4096, group 128, one call per weight set over a
              rotation of distinct weight sets totalling > 2x L2 (a decode
-             step through consecutive layers)
+             step through consecutive layers); the same rotation at M=16
+             and M=128
   w4a4       quantize X (4096 x 8192 fp32) with X.U (rank 32), then the
              block-scaled GEMM against pre-quantized W (8192 x 8192) + XU.V + b
 L2 is flushed (a 256 MiB write) before every op; every op's working set is
@@ -36,6 +37,7 @@ if ROOT not in sys.path:
 METRIC = "INT8/INT4 GEMM TOPS at N=8192 & % tensor peak; W4A16 M=1 HBM GB/s"
 N_SQ = 8192
 W16_N = W16_K = 4096
+W16_MS = (1, 16, 128)
 W4_M, W4_N, W4_K, W4_R = 4096, 8192, 8192, 32
 FLUSH_BYTES = 256 << 20
 
@@ -151,13 +153,14 @@ class Workload:
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         per_set = W16_N * W16_K // 2 + W16_N * (W16_K // 128) * 2
         self.w16_sets = max(8, 2 * l2 // per_set + 2)
-        self.X16 = t(inputs.f16_normal(1, W16_K, 1003))
+        # decode (M=1) plus the M=16 and M=128 shapes of the same layer
+        self.X16 = {m: t(inputs.f16_normal(m, W16_K, 1003)) for m in W16_MS}
         self.W16 = [t(inputs.s4_packed_uniform(W16_N, W16_K, 2003 + 100 * i))
                     for i in range(self.w16_sets)]
         self.S16 = [t(inputs.f16_uniform(W16_N, W16_K // 128, 0.005, 0.02, 3003 + 100 * i))
                     for i in range(self.w16_sets)]
-        self.Y16 = torch.empty((1, W16_N), dtype=torch.float16, device=dev)
-        self.w16_bytes = per_set + 2 * W16_K + 2 * W16_N
+        self.Y16 = {m: torch.empty((m, W16_N), dtype=torch.float16, device=dev) for m in W16_MS}
+        self.w16_bytes = {m: per_set + 2 * m * W16_K + 2 * m * W16_N for m in W16_MS}
 
         # W4A4: weights quantized once (outside any timed region)
         self.X4 = t(inputs.f32_normal(W4_M, W4_K, 1004))
@@ -178,12 +181,14 @@ class Workload:
         torch.cuda.synchronize()
         # The decode rotation is replayed as one CUDA graph (programmatic
         # dependent launch edges are kept), so host launch cost is not timed.
-        self._w4a16_calls()
-        torch.cuda.synchronize()
-        self.w16_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.w16_graph):
-            self._w4a16_calls()
-        torch.cuda.synchronize()
+        self.w16_graph = {}
+        for m in W16_MS:
+            self._w4a16_calls(m)
+            torch.cuda.synchronize()
+            self.w16_graph[m] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.w16_graph[m]):
+                self._w4a16_calls(m)
+            torch.cuda.synchronize()
 
     # each op returns the number of library kernels it launched
     def s8(self):
@@ -198,12 +203,20 @@ class Workload:
         self.qg.gemm_f16(self.Af, self.Bf, C=self.C16)
         return 1
 
-    def _w4a16_calls(self):
+    def _w4a16_calls(self, m):
         for i in range(self.w16_sets):
-            self.qg.w4a16_gemm(self.X16, self.W16[i], self.S16[i], Y=self.Y16)
+            self.qg.w4a16_gemm(self.X16[m], self.W16[i], self.S16[i], Y=self.Y16[m])
 
     def w4a16(self):
-        self.w16_graph.replay()
+        self.w16_graph[1].replay()
+        return self.w16_sets
+
+    def w4a16_m16(self):
+        self.w16_graph[16].replay()
+        return self.w16_sets
+
+    def w4a16_m128(self):
+        self.w16_graph[128].replay()
         return self.w16_sets
 
     def w4a4_quant(self):
@@ -220,7 +233,7 @@ class Workload:
         self.flush_buf.fill_(1)
 
 
-OPS = ["s8", "s4", "f16", "w4a16", "w4a4_quant", "w4a4_gemm"]
+OPS = ["s8", "s4", "f16", "w4a16", "w4a16_m16", "w4a16_m128", "w4a4_quant", "w4a4_gemm"]
 MAIN_KERNEL_OPS = {"s8", "s4", "f16", "w4a4_gemm"}  # ops with a timed tcgen05 GEMM kernel
 
 
@@ -312,7 +325,14 @@ def run_ours(args, rank, world, local_rank):
         s8_tops = world * gemm_ops * args.steps / (float(tt.item()) * 1e-3) / 1e12
 
     w16_call_us = med["w4a16"] * 1e3 / wl.w16_sets
-    w16_gbs = wl.w16_bytes / (w16_call_us * 1e-6) / 1e9
+    w16_gbs = wl.w16_bytes[1] / (w16_call_us * 1e-6) / 1e9
+
+    def w16_line(op, m):
+        us = med[op] * 1e3 / wl.w16_sets
+        gbs = wl.w16_bytes[m] / (us * 1e-6) / 1e9
+        return {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 3), "us_per_call": round(us, 3),
+                "TFLOPS": round(2.0 * m * W16_N * W16_K / (us * 1e-6) / 1e12, 2),
+                "weight_sets": wl.w16_sets}
     breakdown = {
         "int8_gemm_8192": {"TOPS": round(tops(gemm_ops, med["s8"]), 1),
                            "kernel_TOPS": round(tops(gemm_ops, medk["s8"]), 1),
@@ -327,6 +347,8 @@ def run_ours(args, rank, world, local_rank):
         "w4a16_m1_4096": {"GB/s": round(w16_gbs, 1), "us_per_call": round(w16_call_us, 3),
                           "frac_of_hbm": round(w16_gbs / hbm, 3), "weight_sets": wl.w16_sets,
                           "launch": "CUDA graph of the rotation, programmatic dependent launch"},
+        "w4a16_m16_4096": w16_line("w4a16_m16", 16),
+        "w4a16_m128_4096": w16_line("w4a16_m128", 128),
         "w4a4_4096x8192x8192_r32": {
             "quantize_us": round(med["w4a4_quant"] * 1e3, 1),
             "quantize_GB/s": round(W4_M * W4_K * 4 / (med["w4a4_quant"] * 1e-3) / 1e9, 1),
@@ -354,8 +376,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-        "config": {"workload": "INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1 N=K=4096 g128, "
-                               "W4A4 4096x8192x8192 r32 (one step = all six ops)",
+        "config": {"workload": "INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1/16/128 N=K=4096 g128, "
+                               "W4A4 4096x8192x8192 r32 (one step = all eight ops)",
                    "N": N_SQ, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "256 MiB write before every op; every working set > L2",
                    "wall_s_timed_region": round(wall, 3)},

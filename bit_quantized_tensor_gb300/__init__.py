@@ -26,7 +26,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemm.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "qgemm.h")
 
-QG_OK = 0
+(QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_MISALIGNED, QG_ERR_WORKSPACE, QG_ERR_CUDA,
+ QG_ERR_TIMEOUT) = range(7)
 STATUS_NAMES = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED",
                 3: "QG_ERR_MISALIGNED", 4: "QG_ERR_WORKSPACE", 5: "QG_ERR_CUDA",
                 6: "QG_ERR_TIMEOUT"}
@@ -53,6 +54,7 @@ SIGNATURES = {
     "qg_device_status": (_int, [_p]),
     "qg_last_cuda_error": (_int, []),
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
+    "qg_selftest_wait_timeout": (_int, [ctypes.c_uint64, _p]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_gemm_path": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),

@@ -89,6 +89,14 @@ int qg_last_cuda_error(void);
  * the default. */
 int qg_set_timeout_ns(uint64_t ns);
 
+/* Self-test of the failure path (no counterpart on the pages): enqueues one
+ * CTA that waits on an mbarrier nothing arrives on, with a limit of limit_ns
+ * (1 .. 1e9).  The wait runs out, the kernel records QG_ERR_TIMEOUT (call-site
+ * tag 900) in the device status word and returns; qg_device_status() then
+ * reports QG_ERR_TIMEOUT once and clears it.  Nothing faults or traps, and the
+ * context stays usable.  QG_ERR_INVALID_ARG for a limit out of range. */
+int qg_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
 /* Testing hook: K-chunk length of qgemm_s8, in blocks of 64 (1..16, default
  * 16 = 1024).  Every chunk's fp32 partial sums stay within 2^24 for any
  * value in 1..16; shorter chunks only cost more accumulator drains. */
