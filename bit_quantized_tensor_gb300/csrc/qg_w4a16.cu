@@ -30,7 +30,9 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <mutex>
 
+#include "qg_gemm_host.h"
 #include "qg_ptx.cuh"
 
 namespace qg {
@@ -458,6 +460,53 @@ static int launch_w4a16_dec(int M, int N, int K, const __half* X, int64_t ldx, c
 
 }  // namespace qg
 
+#include "w4a16_tc.cuh"
+
+namespace qg {
+
+// Launches w4a16_tc_kernel for batch rows [m0, m0 + 128).
+static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int m0,
+                           const __half* S, __half* Y, int64_t ldy, const Ctl& ctl, int dev,
+                           cudaStream_t s) {
+    using Cfg = W16TcCfg;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                w4a16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                static_cast<int>(w16_tc_smem_bytes(static_cast<int64_t>(Cfg::MAX_GROUPS) * 128)));
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    W16TcParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m0 = m0;
+    p.Y = Y;
+    p.ldy = ldy;
+    p.S = S;
+    p.ctl = ctl;
+    const int tiles = (N + Cfg::BN - 1) / Cfg::BN;
+    const int grid = (tiles + Cfg::CLUSTER - 1) / Cfg::CLUSTER * Cfg::CLUSTER;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = w16_tc_smem_bytes(K);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return map_cuda(cudaLaunchKernelEx(&cfg, w4a16_tc_kernel, tmX, tmW, p));
+}
+
+}  // namespace qg
+
 using namespace qg;
 
 extern "C" {
@@ -496,6 +545,22 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
                                        dec_smem, ctl, s);
         return launch_w4a16_dec<2>(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy, dec_smem,
                                    ctl, s);
+    }
+    // Larger batches: tensor cores, 128 batch rows per launch.
+    if (K / kGroup <= W16TcCfg::MAX_GROUPS) {
+        const int dev = current_device();
+        if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
+        const Ctl ctl = host_ctl(dev);
+        if (!ctl.status) return QG_ERR_CUDA;
+        CUtensorMap tmX, tmW;
+        int rc = make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, ldx * 2, W16TcCfg::BK,
+                              W16TcCfg::BM / W16TcCfg::CLUSTER, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!rc) rc = make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, K / 2, N, K / 2,
+                                   W16TcCfg::BK / 2, W16TcCfg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        for (int64_t r0 = 0; !rc && r0 < M; r0 += W16TcCfg::BM)
+            rc = launch_w4a16_tc(tmX, tmW, static_cast<int>(M), n, k, static_cast<int>(r0), Sh, Yh, ldy,
+                                 ctl, dev, s);
+        return rc;
     }
     // Rows are processed in chunks of up to 128 (8 m16 tiles per CTA).
     for (int64_t r0 = 0; r0 < M; r0 += 128) {
