@@ -5,9 +5,10 @@
 // ("fused-int4-gemm-sm75" README: weight-only int4 with group-128 scales.)
 // Each CTA owns 32 output columns (32 weight rows) for up to 128 batch rows.
 // Per 64-wide K stage:
-//  - X, the operand every CTA needs, is loaded once per cluster of 8 CTAs:
-//    CTA r fetches rows [16 r, 16 r + 16) of the 128 x 64 fp16 tile with a
-//    TMA load multicast to all 8 CTAs (128-byte swizzle);
+//  - X, the operand every CTA needs, is loaded once per cluster of 4 CTAs:
+//    CTA r fetches rows [32 r, 32 r + 32) of the 128 x 64 fp16 tile with a
+//    TMA load multicast to all 4 CTAs (128-byte swizzle).  Clusters of 8
+//    were measured 1.8x slower (CTAs of this size did not all fit at once);
 //  - each CTA fetches its own 32 packed weight rows (32 bytes each);
 //  - four transform warps turn the nibbles into two exact fp16 operand rows
 //    per weight row: q * s_hi and q * s_lo, where s_hi is the group scale with
@@ -20,7 +21,7 @@
 //  - one thread issues tcgen05.mma kind::f16 M=128 N=64 (32 "hi" and 32 "lo"
 //    columns) into a 64-column TMEM accumulator; every product is exact in
 //    fp32, so the only rounding is the fp32 accumulation.  It commits to the
-//    stage-empty barrier of all 8 CTAs, so a stage is refilled only when every
+//    stage-empty barrier of all 4 CTAs, so a stage is refilled only when every
 //    CTA of the cluster has consumed it.
 // The four transform warps then drain TMEM (one lane quadrant each), add the
 // two halves and store fp16 rows.  Scales must stay below 8192 in magnitude
@@ -63,13 +64,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+constexpr uint16_t kClusterMask = 0xF;  // all CTAs of a cluster of 4
+
 struct W16TcCfg {
-    static constexpr int CLUSTER = 8;
+    static constexpr int CLUSTER = 4;
     static constexpr int BM = 128;                      // batch rows per launch
     static constexpr int BN = 32;                       // weight rows (output columns) per CTA
     static constexpr int BK = 64;                       // K per stage: 128 bytes of fp16
     static constexpr int X_BYTES = BM * BK * 2;         // 16 KB
-    static constexpr int X_SLICE = X_BYTES / CLUSTER;   // 16 rows fetched by each CTA
+    static constexpr int X_SLICE = X_BYTES / CLUSTER;   // 32 rows fetched by each CTA
     static constexpr int B_ROWS = 2 * BN;               // q * s_hi rows, then q * s_lo rows
     static constexpr int B_BYTES = B_ROWS * BK * 2;     // 8 KB fp16 operand
     static constexpr int W_BYTES = BN * BK / 2;         // 1 KB packed nibbles
@@ -81,6 +84,7 @@ struct W16TcCfg {
     static constexpr int FIXED_BYTES = STAGES * (X_BYTES + B_BYTES + W_BYTES) + 256 + 1024;
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, BM, B_ROWS);
 
+    static_assert((1 << CLUSTER) - 1 == kClusterMask, "cluster mask");
     static_assert(X_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && X_SLICE % 1024 == 0 && BN % 8 == 0,
                   "swizzle atoms need 1 KB alignment");
     static_assert(NUM_BARRIERS * 8 + 16 <= 256, "barrier area too small");
@@ -174,7 +178,7 @@ __global__ void __cluster_dims__(W16TcCfg::CLUSTER, 1, 1) __launch_bounds__(W16T
             for (int kb = 0; kb < pre; ++kb)
                 tma_load_2d_mc(smem_u32(sX + kb * Cfg::X_BYTES + rank * Cfg::X_SLICE), &tmX, kb * Cfg::BK,
                                p.m0 + static_cast<int>(rank) * (Cfg::BM / Cfg::CLUSTER), full_bar(kb),
-                               0xFF, pol_x);
+                               kClusterMask, pol_x);
             bool ok = true;
             for (int kb = pre; ok && kb < num_kb; ++kb) {
                 const int s = kb % S;
@@ -188,7 +192,7 @@ __global__ void __cluster_dims__(W16TcCfg::CLUSTER, 1, 1) __launch_bounds__(W16T
                             pol_w);
                 tma_load_2d_mc(smem_u32(sX + s * Cfg::X_BYTES + rank * Cfg::X_SLICE), &tmX, kb * Cfg::BK,
                                p.m0 + static_cast<int>(rank) * (Cfg::BM / Cfg::CLUSTER), full_bar(s),
-                               0xFF, pol_x);
+                               kClusterMask, pol_x);
             }
             if (!ok) {
                 // Copies already issued (by this CTA into every CTA of the
@@ -215,7 +219,7 @@ __global__ void __cluster_dims__(W16TcCfg::CLUSTER, 1, 1) __launch_bounds__(W16T
                     tc_mma<MmaKind::F16>(tmem_base, smem_desc_sw128(xa + 32u * k),
                                          smem_desc_sw128(ba + 32u * k), Cfg::IDESC,
                                          (kb > 0 || k > 0) ? 1u : 0u);
-                tc_commit_mc(empty_bar(s), 0xFF);
+                tc_commit_mc(empty_bar(s), kClusterMask);
             }
             tc_commit(accf_bar);  // also when stopped early: lets the epilogue leave
         }
