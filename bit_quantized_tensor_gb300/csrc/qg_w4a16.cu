@@ -475,8 +475,7 @@ static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
             const cudaError_t e = cudaFuncSetAttribute(
-                w4a16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                static_cast<int>(w16_tc_smem_bytes(static_cast<int64_t>(Cfg::MAX_GROUPS) * 128)));
+                w4a16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
             if (e != cudaSuccess) return map_cuda(e);
             attr_set[dev] = true;
         }
@@ -491,11 +490,11 @@ static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M
     p.S = S;
     p.ctl = ctl;
     const int tiles = (N + Cfg::BN - 1) / Cfg::BN;
-    const int grid = (tiles + Cfg::CLUSTER - 1) / Cfg::CLUSTER * Cfg::CLUSTER;
+    const int grid = tiles * Cfg::KSPLIT;  // a cluster per 128 output columns
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(Cfg::THREADS);
-    cfg.dynamicSmemBytes = w16_tc_smem_bytes(K);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -547,14 +546,14 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
                                    ctl, s);
     }
     // Larger batches: tensor cores, 128 batch rows per launch.
-    if (K / kGroup <= W16TcCfg::MAX_GROUPS) {
+    if ((K / kGroup + W16TcCfg::KSPLIT - 1) / W16TcCfg::KSPLIT <= W16TcCfg::MAX_SLICE_GROUPS) {
         const int dev = current_device();
         if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
         const Ctl ctl = host_ctl(dev);
         if (!ctl.status) return QG_ERR_CUDA;
         CUtensorMap tmX, tmW;
         int rc = make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, M, ldx * 2, W16TcCfg::BK,
-                              W16TcCfg::BM / W16TcCfg::CLUSTER, CU_TENSOR_MAP_SWIZZLE_128B);
+                              W16TcCfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (!rc) rc = make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, K / 2, N, K / 2,
                                    W16TcCfg::BK / 2, W16TcCfg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
         for (int64_t r0 = 0; !rc && r0 < M; r0 += W16TcCfg::BM)
