@@ -7,8 +7,9 @@
 // batch rows and splits K four ways: CTA r handles a contiguous quarter of
 // the K groups.  Per 64-wide K stage a CTA
 //  - TMA-loads its 128 x 64 fp16 tile of X and its 128 rows x 32 bytes of
-//    packed weights into a 4-deep ring (covers the memory latency);
-//  - turns the nibbles (eight transform warps) into two exact fp16 operand
+//    packed weights into a 5-deep ring (every cluster re-reads X from L2,
+//    and a load took about 2000 cycles to land under that traffic);
+//  - turns the nibbles into two exact fp16 operand
 //    rows per weight row, q * s_hi and q * s_lo, where s_hi is the group scale
 //    with its three lowest mantissa bits cleared and s_lo = s - s_hi: q has at
 //    most three significant bits, so both products are exact in fp16 and
@@ -16,18 +17,24 @@
 //    dequantize-then-GEMM, costs up to 2^-12 of every weight); the 256 rows go
 //    to the 128-byte-swizzled K-major layout of the MMA's B operand, in a
 //    ring of three slots (with two, the transform of a stage waited for the
-//    MMA two stages back to complete, which paced the loop);
+//    MMA two stages back to complete, which paced the loop).  Two groups of
+//    eight warps take alternate stages: one warp's pass over a stage is
+//    latency-bound (shared-memory loads, the proxy fence, the barrier
+//    arrival), so two stages in flight double the transform rate;
 //  - issues tcgen05.mma kind::f16 M=128 N=256 (one thread) into a 256-column
 //    TMEM accumulator.  Every product is exact in fp32, so the only rounding
 //    is the fp32 accumulation.  Wide MMAs matter here: an instruction costs
 //    about 128 cycles whatever its width, so N=64 ran at a quarter of the rate.
 // At the end every CTA adds its hi and lo halves into a 128 x 128 fp32
-// partial tile in shared memory; after a cluster barrier CTA r sums rows
-// [32 r, 32 r + 32) of the four partial tiles through distributed shared
-// memory and stores them as fp16.  Weight rows and scales are fetched before
-// the programmatic dependent wait; X after it.  Every wait is bounded; the
-// CTAs of a cluster leave only after a second cluster barrier.  Scales must
-// stay below 8192 in magnitude (8 * s_hi must be a finite fp16).
+// partial tile in shared memory and, once every CTA of the cluster is past
+// its K loop, bulk-copies rows [32 r, 32 r + 32) of it into CTA r's shared
+// memory (the copy engine signals CTA r's barrier with the byte count); CTA r
+// adds the four partials of its rows and stores them as fp16.  Both cluster
+// barriers are relaxed: the copies carry their own completion, and a barrier
+// with release semantics cost about half a microsecond here, as much as the
+// whole exchange.  Weight rows and scales are fetched before the
+// programmatic dependent wait; X after it.  Every wait is bounded.  Scales
+// must stay below 8192 in magnitude (8 * s_hi must be a finite fp16).
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -43,14 +50,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 16-byte load from the shared memory of another CTA of the cluster.
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
+// Execution barrier over all threads of the cluster, without memory ordering.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of a CTA of the cluster; completes on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
 }
 
 struct W16TcCfg {
@@ -62,25 +75,31 @@ struct W16TcCfg {
     static constexpr int B_ROWS = 2 * BN;               // q * s_hi rows, then q * s_lo rows
     static constexpr int B_BYTES = B_ROWS * BK * 2;     // 32 KB fp16 operand
     static constexpr int W_BYTES = BN * BK / 2;         // 4 KB packed nibbles
-    static constexpr int STAGES = 4;                    // X + packed-weight ring (memory latency)
+    static constexpr int STAGES = 5;                    // X + packed-weight ring (memory latency)
     static constexpr int BSLOTS = 3;                    // B operand ring (transform -> MMA)
-    static constexpr int XFORM_WARPS = 8;
+    static constexpr int XFORM_WARPS = 16;
+    static constexpr int XFORM_GROUPS = 2;              // groups of warps on alternate stages
+    static constexpr int GROUP_WARPS = XFORM_WARPS / XFORM_GROUPS;
     static constexpr int THREADS = 32 * (2 + XFORM_WARPS);  // producer, MMA, transform/epilogue
     static constexpr int TMEM_COLS = 256;
     static constexpr int MAX_SLICE_GROUPS = 64;         // K groups per quarter: K <= 32768
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * BSLOTS + 1;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * BSLOTS + 2;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SCALE_BYTES = BN * MAX_SLICE_GROUPS * 2;  // 16 KB
     static constexpr int RING_BYTES = STAGES * (X_BYTES + W_BYTES) + BSLOTS * B_BYTES;
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + SCALE_BYTES + 1024;
     static constexpr int RED_STRIDE = BN + 4;           // floats per partial-tile row (bank spread)
+    static constexpr int SLICE_ROWS = BM / KSPLIT;      // output rows each CTA finishes
+    static constexpr int SLICE_BYTES = SLICE_ROWS * RED_STRIDE * 4;  // one bulk copy
+    static constexpr int RX_OFF = (BM * RED_STRIDE * 4 + 1023) / 1024 * 1024;  // received partials
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, BM, B_ROWS);
 
     static_assert(X_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
                   "swizzle atoms need 1 KB alignment");
     static_assert(NUM_BARRIERS * 8 + 16 <= BAR_BYTES, "barrier area too small");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget exceeded");
-    static_assert(BM * RED_STRIDE * 4 <= RING_BYTES, "partial tile reuses the rings");
+    static_assert(RX_OFF + KSPLIT * SLICE_BYTES <= RING_BYTES, "partial tiles reuse the rings");
+    static_assert(SLICE_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 
 struct W16TcParams {
@@ -98,6 +117,7 @@ enum W16TcSite : int {
     kSiteW16TcReady = 313,
     kSiteW16TcXform = 314,
     kSiteW16TcAcc = 315,
+    kSiteW16TcRx = 316,
 };
 
 __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16TcCfg::THREADS, 1)
@@ -121,6 +141,7 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
     auto ready_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };  // B slot b written
     auto bfree_bar = [&](int b) { return bar0 + 8u * (2 * S + NB + b); };  // MMA done with B slot b
     const uint32_t accf_bar = bar0 + 8u * (2 * S + 2 * NB);
+    const uint32_t rx_bar = bar0 + 8u * (2 * S + 2 * NB + 1);  // partials of this CTA's rows arrived
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -140,10 +161,11 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < NB; ++b) {
-            mbar_init(ready_bar(b), Cfg::XFORM_WARPS);
+            mbar_init(ready_bar(b), Cfg::GROUP_WARPS);  // one group transforms a stage
             mbar_init(bfree_bar(b), 1);
         }
         mbar_init(accf_bar, 1);
+        mbar_init(rx_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmX);
@@ -221,16 +243,18 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
         }
     } else {
         // ---------------------------------------- transform, then epilogue
-        const int tid = threadIdx.x - 64;                 // 0..255
+        const int tid = threadIdx.x - 64;                 // 0..511
         for (int i = tid; i < Cfg::BN * ng; i += 32 * Cfg::XFORM_WARPS) {  // this quarter's scales
             const int r = i / ng, gi = i - r * ng;
             sS[r * Cfg::MAX_SLICE_GROUPS + gi] =
                 (n0 + r < p.N) ? __half_as_ushort(p.S[static_cast<int64_t>(n0 + r) * G + g_beg + gi]) : 0;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::XFORM_WARPS) : "memory");
-        const int r = tid >> 1, q = tid & 1;              // weight row, 32-value half of the stage
+        const int grp = (warp - 2) / Cfg::GROUP_WARPS;    // stages grp, grp + 2, ...
+        const int gt = tid - grp * 32 * Cfg::GROUP_WARPS;  // 0..255 within the group
+        const int r = gt >> 1, q = gt & 1;                // weight row, 32-value half of the stage
         const uint32_t bw = (r >> 3) * 1024 + (r & 7) * 128;  // row start in the swizzled B stage
-        for (int i = 0; i < num_kb; ++i) {
+        for (int i = grp; i < num_kb; i += Cfg::XFORM_GROUPS) {
             const int s = i % S, b = i % NB;
             const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
             // the weights of stage i have landed and the MMA is done with the
@@ -260,9 +284,9 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const __half2 qv = *reinterpret_cast<const __half2*>(&nat[j]);
-                    __half2 a = __hmul2(qv, shi2), b = __hmul2(qv, slo2);
+                    __half2 a = __hmul2(qv, shi2), c = __hmul2(qv, slo2);
                     hi[j] = *reinterpret_cast<uint32_t*>(&a);
-                    lo[j] = *reinterpret_cast<uint32_t*>(&b);
+                    lo[j] = *reinterpret_cast<uint32_t*>(&c);
                 }
                 const int c = 4 * q + h;                   // 16-byte chunk: k = 8c .. 8c + 7
                 const uint32_t off = static_cast<uint32_t>((c ^ (r & 7)) << 4);
@@ -274,72 +298,80 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
             __syncwarp();
             if (lane == 0) mbar_arrive(ready_bar(b));
         }
-        // partial tile: TMEM lanes 32 (warp % 4) .. + 32, columns [64 ch, 64 ch + 64)
-        // (hi) and [128 + 64 ch, ...) (lo), added and stored to shared memory
+        // partial tile: TMEM lanes 32 (warp % 4) .. + 32, columns [32 ch, 32 ch + 32)
+        // (hi) and [128 + 32 ch, ...) (lo), added and stored to shared memory
         const bool got = bounded_wait(accf_bar, 0u, nullptr, p.ctl, kSiteW16TcAcc);
         const int quad = warp & 3, ch = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::XFORM_WARPS) : "memory");  // stages no longer read
         const bool have = ok && __all_sync(0xffffffffu, got) && !*abort_flag && num_kb > 0;
-        if (have) tc_fence_after();
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            uint32_t vh[32], vl[32];
-            if (have) {
-                const uint32_t ta = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                    static_cast<uint32_t>(64 * ch + 32 * part);
-                tmem_ld_32x32b_x32(ta, vh);
-                tmem_ld_32x32b_x32(ta + 128u, vl);
-                tmem_wait_ld();
-            }
-            float* dst = red + row * Cfg::RED_STRIDE + 64 * ch + 32 * part;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (have)
-                    v = make_float4(__uint_as_float(vh[j]) + __uint_as_float(vl[j]),
-                                    __uint_as_float(vh[j + 1]) + __uint_as_float(vl[j + 1]),
-                                    __uint_as_float(vh[j + 2]) + __uint_as_float(vl[j + 2]),
-                                    __uint_as_float(vh[j + 3]) + __uint_as_float(vl[j + 3]));
-                *reinterpret_cast<float4*>(dst + j) = v;
-            }
+        uint32_t vh[32], vl[32];
+        if (have) {
+            tc_fence_after();
+            const uint32_t ta = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                static_cast<uint32_t>(32 * ch);
+            tmem_ld_32x32b_x32(ta, vh);
+            tmem_ld_32x32b_x32(ta + 128u, vl);
+            tmem_wait_ld();
         }
+        float* dst = red + row * Cfg::RED_STRIDE + 32 * ch;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (have)
+                v = make_float4(__uint_as_float(vh[j]) + __uint_as_float(vl[j]),
+                                __uint_as_float(vh[j + 1]) + __uint_as_float(vl[j + 1]),
+                                __uint_as_float(vh[j + 2]) + __uint_as_float(vl[j + 2]),
+                                __uint_as_float(vh[j + 3]) + __uint_as_float(vl[j + 3]));
+            *reinterpret_cast<float4*>(dst + j) = v;
+        }
+        fence_proxy_async_smem();  // the bulk copies read these rows
     }
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the four partial tiles are complete
-    if (warp >= 2) {
-        // rows [32 rank, 32 rank + 32) of the sum of the four partial tiles
-        const int tid = threadIdx.x - 64;
-        const uint32_t red_local = smem_u32(red);
-        uint32_t peer[Cfg::KSPLIT];
-#pragma unroll
-        for (int c = 0; c < Cfg::KSPLIT; ++c) peer[c] = mapa_shared(red_local, static_cast<uint32_t>(c));
-        float4 part[4][Cfg::KSPLIT];                      // all remote loads first, then the sums
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = tid + 256 * e;                // 32 rows x 32 four-column chunks
-            const int trow = static_cast<int>(rank) * 32 + (idx >> 5);  // row of the 128-row tile
-            const uint32_t off = static_cast<uint32_t>((trow * Cfg::RED_STRIDE + 4 * (idx & 31)) * 4);
-#pragma unroll
-            for (int c = 0; c < Cfg::KSPLIT; ++c) part[e][c] = ld_shared_cluster_f4(peer[c] + off);
+    if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(rx_bar, static_cast<uint32_t>((Cfg::KSPLIT - 1) * Cfg::SLICE_BYTES));
+    // every CTA of the cluster is past its K loop: its rings, where the
+    // partials land, are free (all MMAs, hence all their operand reads, done)
+    cluster_sync_relaxed();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+    const uint32_t red_u32 = smem_u32(red), rx_u32 = smem_u32(smem + Cfg::RX_OFF);
+    if (threadIdx.x == 0) {
+        for (int d = 1; d < Cfg::KSPLIT; ++d) {  // rows of CTA `dst` into its slot `rank`
+            const uint32_t dst = (rank + static_cast<uint32_t>(d)) % Cfg::KSPLIT;
+            bulk_copy_s2cluster(mapa_shared(rx_u32 + rank * Cfg::SLICE_BYTES, dst),
+                                red_u32 + dst * Cfg::SLICE_BYTES, Cfg::SLICE_BYTES, mapa_shared(rx_bar, dst));
         }
+    }
+    if (warp >= 2) {
+        // rows [32 rank, 32 rank + 32): own partial plus the three received
+        const int tid = threadIdx.x - 64;
+        const bool got = bounded_wait(rx_bar, 0u, nullptr, p.ctl, kSiteW16TcRx);
+        const float* own = red + static_cast<int>(rank) * Cfg::SLICE_ROWS * Cfg::RED_STRIDE;
+        const float* rx = reinterpret_cast<const float*>(smem + Cfg::RX_OFF);
+        constexpr int E = Cfg::SLICE_ROWS * (Cfg::BN / 4) / (32 * Cfg::XFORM_WARPS);  // float4s per thread
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = tid + 256 * e;
-            const int trow = static_cast<int>(rank) * 32 + (idx >> 5);
-            const int c4 = idx & 31;
-            float4 sum = part[e][0];
+        for (int e = 0; e < E; ++e) {
+            const int idx = tid + 32 * Cfg::XFORM_WARPS * e;  // 32 rows x 32 four-column chunks
+            const int t = idx >> 5, c4 = idx & 31;
+            const int o = t * Cfg::RED_STRIDE + 4 * c4;
+            float4 sum = *reinterpret_cast<const float4*>(own + o);
 #pragma unroll
-            for (int c = 1; c < Cfg::KSPLIT; ++c) {
-                sum.x += part[e][c].x;
-                sum.y += part[e][c].y;
-                sum.z += part[e][c].z;
-                sum.w += part[e][c].w;
+            for (int c = 0; c < Cfg::KSPLIT; ++c) {
+                if (c == static_cast<int>(rank)) continue;
+                const float4 v = *reinterpret_cast<const float4*>(rx + c * (Cfg::SLICE_BYTES / 4) + o);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
             }
-            const int m = p.m0 + trow, col = n0 + 4 * c4;
-            if (m < p.M && col < p.N) {
+            const int m = p.m0 + static_cast<int>(rank) * Cfg::SLICE_ROWS + t, col = n0 + 4 * c4;
+            if (got && m < p.M && col < p.N) {
                 __half* dst = p.Y + static_cast<int64_t>(m) * p.ldy + col;
                 if (col + 4 <= p.N && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
                     __half2 a = __floats2half2_rn(sum.x, sum.y), b = __floats2half2_rn(sum.z, sum.w);
@@ -352,12 +384,9 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
             }
         }
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its partial tile
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
-    }
+    // a CTA's outgoing copies have been read once every destination has
+    // seen its barrier complete: only then may the source CTA leave
+    cluster_sync_relaxed();
 }
 
 }  // namespace qg
