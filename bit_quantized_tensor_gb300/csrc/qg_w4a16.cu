@@ -416,6 +416,250 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
 }
 
+// ------------------------------------------------- decode, M <= 8 (GEMV)
+//
+// A chain of decode calls (one layer after another) is bound by two things:
+// streaming the packed weights, and the latency of each call after the
+// previous one has finished (griddepcontrol.wait returns ~0.7 us after the
+// last CTA of the previous grid has left).  This kernel is shaped so that the
+// first overlaps the second:
+//  - one CTA per SM, using at most half of the SM (512 threads, <= 64
+//    registers, <= ~110 KB of shared memory), so the next call's CTAs are
+//    resident while this call computes and their weight rows (bulk copies)
+//    and scales are in flight before this call ends; the CTA owns R
+//    consecutive weight rows (R = N / #SMs rounded up, at most 32) and all
+//    of K;
+//  - the work after the wait is cut to the arithmetic that needs X.  A
+//    nibble n (offset binary, v + 8) masked into the low mantissa bits of a
+//    zero-exponent fp16 word IS the fp16 subnormal n * 2^-24: no exponent
+//    OR, no subtraction, so a 32-bit word of 8 weights costs one shift and
+//    four lop3 (even k at bits 0-3 of each half: n * 2^-24; odd k at bits
+//    4-7: 16 n * 2^-24).  Even and odd k go to separate MMAs and
+//    accumulators (the odd one carries the factor 16), and the offset 8 is
+//    removed exactly by starting each group's even accumulator at
+//    -8 * 2^-24 * sum(x over the group), computed once per call when X is
+//    staged.  Every product is exact (an 11-bit by 4-bit product in fp32);
+//    the scale s * 2^24 (even) and s * 2^20 (odd) is applied in fp32 per
+//    group, as in the other W4A16 kernels.
+//  - X (M x K) is staged once into shared memory, already permuted into the
+//    MMA's pair order, together with the group sums.
+// With T m16 tiles per CTA, warp w works on tile w / (16 / T) and on every
+// (16 / T)-th group; rows past the CTA's are computed on its last row's data
+// and never stored, batch columns past M read a zero slot, so the loop has no
+// predicated loads.  The warps' partial tiles are added through shared memory
+// in one pass.
+constexpr int kD1Warps = 16;
+constexpr int kD1Threads = 32 * kD1Warps;
+constexpr int kD1MaxRows = 32;                  // two m16 tiles
+constexpr size_t kD1Budget = 110 * 1024;        // two calls' CTAs share an SM
+constexpr int kSiteW16D1Bulk = 303;
+constexpr int kSiteW16D1Drain = 304;
+
+// Shared-memory layout of k_w4a16_gemv for R rows, M batch rows, K.
+struct D1Layout {
+    int64_t wrs;        // bytes per staged weight row (K/2 + 64: rows g and g+8 on other banks)
+    int64_t xrs;        // 16-byte slots per staged X row (16 per group + 4)
+    int64_t srs;        // floats per scale row (2 per group + 2)
+    int64_t w_off, x_off, c_off, s_off, red_off, bytes;
+};
+inline D1Layout d1_layout(int64_t M, int64_t K, int64_t R) {
+    D1Layout L;
+    const int64_t G = K / 128;
+    L.wrs = K / 2 + 64;
+    L.xrs = G * 16 + 4;
+    L.srs = 2 * G + 2;
+    L.w_off = 0;
+    L.x_off = L.w_off + R * L.wrs;
+    L.c_off = L.x_off + (M * L.xrs + 1) * 16;  // + one zero slot
+    L.s_off = L.c_off + G * 8 * 4;
+    L.red_off = L.s_off + ((R * L.srs * 4 + 15) / 16) * 16;
+    L.bytes = L.red_off + static_cast<int64_t>(kD1Warps) * 16 * M * 4;
+    return L;
+}
+
+// The same layout narrowed for the kernel (all offsets below the budget).
+struct D1Off {
+    int wrs, xrs, srs, x_off, c_off, s_off, red_off;
+};
+inline D1Off d1_off(const D1Layout& L) {
+    return D1Off{static_cast<int>(L.wrs), static_cast<int>(L.xrs), static_cast<int>(L.srs),
+                 static_cast<int>(L.x_off), static_cast<int>(L.c_off), static_cast<int>(L.s_off),
+                 static_cast<int>(L.red_off)};
+}
+
+// d = a . b + c (m16n8k16, fp16 inputs, fp32 accumulators), c separate from d.
+__device__ __forceinline__ void mma_16816_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                            float c0, float c1, float c2, float c3) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+// (a ^ c) & b: the nibbles under mask b, XORed with 8 (two's complement ->
+// offset binary), nothing else: an fp16 subnormal n * 2^-24 (or 16 n * 2^-24).
+__device__ __forceinline__ uint32_t nib_sub(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x48;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int T>  // m16 tiles per CTA (R <= 16 T)
+__global__ void __launch_bounds__(kD1Threads, 2)
+    k_w4a16_gemv(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
+                 const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
+                 int64_t ldy, int R, const D1Off L, const Ctl ctl) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int failed;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup, K8 = K / 8;
+    const int n0 = blockIdx.x * R;
+    const int rows = min(R, N - n0);
+    uint8_t* ws = dsm;
+    uint4* xs = reinterpret_cast<uint4*>(dsm + L.x_off);
+    float* cs = reinterpret_cast<float*>(dsm + L.c_off);
+    float* sp = reinterpret_cast<float*>(dsm + L.s_off);
+    float* red = reinterpret_cast<float*>(dsm + L.red_off);
+    const uint32_t bar = smem_u32(&wbar);
+
+    if (threadIdx.x == 0) {
+        failed = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {  // the CTA's weight rows, one bulk copy per row
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * (K / 2));
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_copy_g2s(smem_u32(ws + r * L.wrs), Wq + static_cast<int64_t>(n0 + r) * (K / 2),
+                          static_cast<uint32_t>(K / 2), bar);
+    }
+    pdl_launch_dependents();
+    // scales in fp32, pre-multiplied by 2^24 (even k) and 2^20 (odd k)
+    for (int i = threadIdx.x; i < rows * G; i += kD1Threads) {
+        const int r = i / G, gi = i - r * G;
+        const float sc = __half2float(__ushort_as_half(ld_nc_u16(S + static_cast<int64_t>(n0 + r) * G + gi)));
+        *reinterpret_cast<float2*>(sp + r * L.srs + 2 * gi) = make_float2(sc * 16777216.f, sc * 1048576.f);
+    }
+
+    // X may be the previous kernel's output: read it only now.
+    pdl_wait_prior_grid();
+    // Stage X: chunk j = 8 consecutive k of row m, stored as the pairs
+    // (x0,x4) (x2,x6) (x1,x5) (x3,x7) at slot (g_i * 4 + i) * 4 + t of row m,
+    // where k = 128 g_i + 32 t + 8 i; 16 consecutive chunks make a group,
+    // whose sum (fp32, fixed order) gives the even accumulator's start.
+    for (int m = 0; m < M; ++m) {
+        const __half* xr = X + static_cast<int64_t>(m) * ldx;
+        uint4* xsr = xs + m * L.xrs;
+        for (int cb = warp * 32; cb < K8; cb += kD1Threads) {  // whole warps: the sums shuffle
+            const int c8 = cb + lane;
+            const bool ok = c8 < K8;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (ok) v = __ldg(reinterpret_cast<const uint4*>(xr + 8 * c8));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[q]));
+                sum += f.x;
+                sum += f.y;
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            if (ok) {
+                const int gi = c8 >> 4, u = c8 & 15;
+                xsr[(gi * 4 + (u & 3)) * 4 + (u >> 2)] =
+                    make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.y, v.w, 0x5410),
+                               __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x7632));
+                if (u == 0) cs[gi * 8 + m] = -4.76837158203125e-07f * sum;  // -8 * 2^-24
+            }
+        }
+    }
+    for (int i = threadIdx.x; i < G * 8; i += kD1Threads)  // batch columns past M
+        if ((i & 7) >= M) cs[i] = 0.f;
+    if (threadIdx.x == 0) xs[L.xrs * M] = make_uint4(0u, 0u, 0u, 0u);
+    if (!bounded_wait(bar, 0u, nullptr, ctl, kSiteW16D1Bulk)) {
+        failed = 1;
+        if (lane == 0) bounded_wait(bar, 0u, nullptr, ctl, kSiteW16D1Drain);
+    }
+    __syncthreads();  // X, group sums and (unless failed) weights staged
+
+    // warp w: tile w / WPT, groups w % WPT, w % WPT + WPT, ...
+    constexpr int WPT = kD1Warps / T;
+    const int tt = warp / WPT, gw = warp - tt * WPT;
+    // Rows past the CTA's are computed on the data of its last row and never
+    // stored; batch columns past M read a zero slot.
+    const int r0 = min(16 * tt + g, rows - 1), r1 = min(16 * tt + g + 8, rows - 1);
+    const uint8_t* wrow0 = ws + r0 * L.wrs + 16 * t;
+    const uint8_t* wrow1 = ws + r1 * L.wrs + 16 * t;
+    const float* srow0 = sp + r0 * L.srs;
+    const float* srow1 = sp + r1 * L.srs;
+    const uint4* xbase = g < M ? xs + g * L.xrs + t : xs + L.xrs * M;  // zero slot after the rows
+    const int xstep = g < M ? 4 : 0, xgs = g < M ? 16 : 0;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int gi = gw; gi < G; gi += WPT) {
+        const uint4* xrow = xbase + xgs * gi;
+        const float2 cc = *reinterpret_cast<const float2*>(cs + gi * 8 + 2 * t);
+        const uint4 w0 = *reinterpret_cast<const uint4*>(wrow0 + gi * 64);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(wrow1 + gi * 64);
+        const float2 s0 = *reinterpret_cast<const float2*>(srow0 + 2 * gi);
+        const float2 s1 = *reinterpret_cast<const float2*>(srow1 + 2 * gi);
+        float ae[4], ao[4];
+        const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w}, wb[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t ha = wa[i] >> 8, hb = wb[i] >> 8;
+            const uint32_t ev[4] = {nib_sub(wa[i], 0x000F000Fu, 0x00080008u), nib_sub(wb[i], 0x000F000Fu, 0x00080008u),
+                                    nib_sub(ha, 0x000F000Fu, 0x00080008u), nib_sub(hb, 0x000F000Fu, 0x00080008u)};
+            const uint32_t od[4] = {nib_sub(wa[i], 0x00F000F0u, 0x00800080u), nib_sub(wb[i], 0x00F000F0u, 0x00800080u),
+                                    nib_sub(ha, 0x00F000F0u, 0x00800080u), nib_sub(hb, 0x00F000F0u, 0x00800080u)};
+            const uint4 xf = xrow[xstep * i];
+            if (i == 0) {
+                mma_16816_c(ae, ev, xf.x, xf.y, cc.x, cc.y, cc.x, cc.y);
+                mma_16816_c(ao, od, xf.z, xf.w, 0.f, 0.f, 0.f, 0.f);
+            } else {
+                mma_16816(ae, ev, xf.x, xf.y);
+                mma_16816(ao, od, xf.z, xf.w);
+            }
+        }
+        y[0] = fmaf(s0.y, ao[0], fmaf(s0.x, ae[0], y[0]));
+        y[1] = fmaf(s0.y, ao[1], fmaf(s0.x, ae[1], y[1]));
+        y[2] = fmaf(s1.y, ao[2], fmaf(s1.x, ae[2], y[2]));
+        y[3] = fmaf(s1.y, ao[3], fmaf(s1.x, ae[3], y[3]));
+    }
+
+    // partial tiles: red[warp][row][m] (the warp's tile), batch columns < M only
+    {
+        float* rw = red + warp * 16 * M;
+        if (2 * t < M) {
+            rw[g * M + 2 * t] = y[0];
+            rw[(g + 8) * M + 2 * t] = y[2];
+        }
+        if (2 * t + 1 < M) {
+            rw[g * M + 2 * t + 1] = y[1];
+            rw[(g + 8) * M + 2 * t + 1] = y[3];
+        }
+    }
+    __syncthreads();
+    if (failed) return;
+    // output (m, r): sum of the WPT partials of r's tile, in warp order
+    for (int m = 0; m < M; ++m)
+        for (int r = threadIdx.x; r < rows; r += kD1Threads) {
+            const float* pr = red + ((r >> 4) * WPT * 16 + (r & 15)) * M + m;
+            float v[WPT];
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) v[w] = pr[w * 16 * M];
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) sum += v[w];
+            Y[static_cast<int64_t>(m) * ldy + n0 + r] = __float2half_rn(sum);
+        }
+}
+
 static std::atomic<int> g_w4a16_pdl{1};
 
 template <int MT, int NT>
@@ -458,6 +702,46 @@ static int launch_w4a16_dec(int M, int N, int K, const __half* X, int64_t ldx, c
     return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_dec<MB>, M, N, K, X, ldx, Wq, S, Y, ldy, ctl));
 }
 
+// Rows per CTA of k_w4a16_gemv, or 0 when its staging does not fit.
+static int d1_rows(int64_t M, int64_t N, int64_t K, int dev) {
+    if (M > 8) return 0;
+    const int64_t sms = num_sms(dev);
+    int64_t R = (N + sms - 1) / sms;
+    if (R > kD1MaxRows) R = kD1MaxRows;
+    while (R > 1 && static_cast<size_t>(d1_layout(M, K, R).bytes) > kD1Budget) --R;
+    if (static_cast<size_t>(d1_layout(M, K, R).bytes) > kD1Budget) return 0;
+    return static_cast<int>(R);
+}
+
+static int launch_w4a16_gemv(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
+                             const __half* S, __half* Y, int64_t ldy, int R, const Ctl& ctl,
+                             cudaStream_t s) {
+    static std::atomic<int> attr_done{0};
+    if (!attr_done.load()) {
+        cudaError_t e = cudaFuncSetAttribute(k_w4a16_gemv<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kD1Budget));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_w4a16_gemv<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kD1Budget));
+        if (e != cudaSuccess) return map_cuda(e);
+        attr_done.store(1);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + R - 1) / R));
+    cfg.blockDim = dim3(kD1Threads);
+    const D1Layout lay = d1_layout(M, K, R);
+    const D1Off off = d1_off(lay);
+    cfg.dynamicSmemBytes = static_cast<size_t>(lay.bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (R > 16)
+        return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv<2>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
+    return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv<1>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
+}
 }  // namespace qg
 
 #include "w4a16_tc.cuh"
@@ -533,6 +817,17 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
     const int n = static_cast<int>(N), k = static_cast<int>(K);
     // Decode shapes: weight slab bulk-copied and X staged in shared memory,
     // weights as the A operand.
+    // GEMV shapes: one CTA per SM, half an SM each, so consecutive calls overlap.
+    if (M <= 8) {
+        const int dev = current_device();
+        if (dev < 0) return QG_ERR_CUDA;
+        const int R = d1_rows(M, N, K, dev);
+        if (R > 0) {
+            const Ctl ctl = host_ctl(dev);
+            if (!ctl.status) return QG_ERR_CUDA;
+            return launch_w4a16_gemv(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy, R, ctl, s);
+        }
+    }
     const size_t dec_smem = dec_smem_bytes(M, K);
     if (M <= 16 && dec_smem <= kDecMaxSmem) {
         const int dev = current_device();
