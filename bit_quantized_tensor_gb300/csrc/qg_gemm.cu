@@ -203,79 +203,157 @@ int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, 
 }
 
 // -------------------------------------------------------- operand converters
+//
+// Both converters expand 16 source bytes into 32 destination bytes (int8 ->
+// fp16; two packed nibbles -> two e4m3 bytes), so one kernel shape serves
+// both: threads over the 16-byte chunks of a row, CTAs strided over rows,
+// blockIdx.z selecting the operand (A and B in one launch).  Both are
+// HBM-bound: 3 bytes of traffic per int8 value, 1.5 per int4 value.
 
-// int8 -> fp16, 16 elements per thread; cols is a multiple of 16.
-__global__ void k_s8_to_f16(const int8_t* __restrict__ src, int64_t rows, int64_t cols, int64_t lds,
-                            __half* __restrict__ dst, int64_t ldd) {
-    const int64_t per_row = cols / 16;
-    const int64_t total = rows * per_row;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / per_row;
-        const int64_t c = (i - r * per_row) * 16;
-        const int4 v = __ldg(reinterpret_cast<const int4*>(src + r * lds + c));
-        const int8_t* b = reinterpret_cast<const int8_t*>(&v);
-        uint4 o[2];
-        __half2* h = reinterpret_cast<__half2*>(o);
+struct ExpandJob {
+    const uint8_t* src;
+    int64_t rows, lds;  // source row stride in bytes
+    uint8_t* dst;
+    int64_t ldd;        // destination row stride in bytes
+};
+struct ExpandJobs {
+    ExpandJob job[2];
+    int64_t chunks;     // 16-byte source chunks per row (same for every job)
+};
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// int8 -> fp16, exact: the byte XOR 0x80 (offset binary, 0..255) placed under
+// the fp16 exponent of 1024 is 1024 + b + 128; subtracting 1152 leaves b.
+struct S8ToF16 {
+    __device__ __forceinline__ void operator()(const uint4& in, uint4 (&out)[2]) const {
+        const __half2 c1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        const uint32_t w[4] = {in.x ^ 0x80808080u, in.y ^ 0x80808080u, in.z ^ 0x80808080u,
+                               in.w ^ 0x80808080u};
+        uint32_t o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            h[j] = __halves2half2(__short2half_rn(b[2 * j]), __short2half_rn(b[2 * j + 1]));
-        uint4* d = reinterpret_cast<uint4*>(dst + r * ldd + c);
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = __byte_perm(w[q], 0x64646464u, 0x4140);  // bytes 0, 1
+            const uint32_t hi = __byte_perm(w[q], 0x64646464u, 0x4342);  // bytes 2, 3
+            __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), c1152);
+            __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), c1152);
+            o[2 * q] = *reinterpret_cast<uint32_t*>(&a);
+            o[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+};
+
+// Signed nibble (low nibble = even k) -> e4m3 byte, exact for -8..7.  Four
+// nibbles (16 bits) are a prmt selector: with table P = e4m3(0..7) a
+// selector n < 8 picks P[n], and n >= 8 (bit 3 = sign-replicate mode) gives
+// 0x00 because every P entry is positive; with the selector's bit 3 flipped
+// and table Q[i] = e4m3(8 - i), the magnitude of n - 16 = -(8 - (n & 7)),
+// n >= 8 picks Q[n & 7] and n < 8 gives 0x00.  The sign bit is set on the
+// nonzero bytes of the second lookup (all Q entries are nonzero and below
+// 0x80, so the per-byte add cannot carry).  The tables come from the
+// hardware float -> e4m3 conversion.
+struct S4ToE4M3 {
+    uint32_t p_lo, p_hi, q_lo, q_hi;
+    __device__ __forceinline__ S4ToE4M3() {
+        p_lo = p_hi = q_lo = q_hi = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t pc = static_cast<uint8_t>(__nv_cvt_float_to_fp8(static_cast<float>(i), __NV_SATFINITE, __NV_E4M3));
+            const uint32_t qc = static_cast<uint8_t>(__nv_cvt_float_to_fp8(static_cast<float>(8 - i), __NV_SATFINITE, __NV_E4M3));
+            if (i < 4) {
+                p_lo |= pc << (8 * i);
+                q_lo |= qc << (8 * i);
+            } else {
+                p_hi |= pc << (8 * (i - 4));
+                q_hi |= qc << (8 * (i - 4));
+            }
+        }
+    }
+    // prmt in its default mode: bit 3 of a selector nibble replicates the
+    // selected byte's sign (the __byte_perm intrinsic ignores that bit).
+    __device__ __forceinline__ static uint32_t prmt_sign(uint32_t a, uint32_t b, uint32_t sel) {
+        uint32_t d;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+        return d;
+    }
+    __device__ __forceinline__ uint32_t four(uint32_t sel) const {
+        const uint32_t pos = prmt_sign(p_lo, p_hi, sel);
+        const uint32_t mag = prmt_sign(q_lo, q_hi, sel ^ 0x8888u);
+        const uint32_t sign = (mag + 0x7F7F7F7Fu) & 0x80808080u;
+        return pos | mag | sign;
+    }
+    __device__ __forceinline__ void operator()(const uint4& in, uint4 (&out)[2]) const {
+        out[0] = make_uint4(four(in.x & 0xFFFFu), four(in.x >> 16), four(in.y & 0xFFFFu), four(in.y >> 16));
+        out[1] = make_uint4(four(in.z & 0xFFFFu), four(in.z >> 16), four(in.w & 0xFFFFu), four(in.w >> 16));
+    }
+};
+
+template <class Conv>
+__global__ void __launch_bounds__(256) k_expand(const ExpandJobs jobs) {
+    const ExpandJob jb = blockIdx.z == 0 ? jobs.job[0] : jobs.job[1];  // no dynamic index into parameters
+    const Conv conv;
+    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (c >= jobs.chunks) return;
+    // four rows per pass, loads first: 64 bytes in flight per thread
+    constexpr int U = 4;
+    const int64_t step = gridDim.y;
+    int64_t r = blockIdx.y;
+    for (; r + (U - 1) * step < jb.rows; r += U * step) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = ld_stream16(jb.src + (r + u * step) * jb.lds + 16 * c);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint4 o[2];
+            conv(v[u], o);
+            uint4* d = reinterpret_cast<uint4*>(jb.dst + (r + u * step) * jb.ldd + 32 * c);
+            d[0] = o[0];
+            d[1] = o[1];
+        }
+    }
+    for (; r < jb.rows; r += step) {
+        const uint4 v = ld_stream16(jb.src + r * jb.lds + 16 * c);
+        uint4 o[2];
+        conv(v, o);
+        uint4* d = reinterpret_cast<uint4*>(jb.dst + r * jb.ldd + 32 * c);
         d[0] = o[0];
         d[1] = o[1];
     }
 }
 
-// Packed signed 4-bit (low nibble = even k) -> one e4m3 byte per value.
-// 16 packed bytes (32 values) per thread; bytes_per_row is a multiple of 16.
-__global__ void k_s4_to_e4m3(const uint8_t* __restrict__ src, int64_t rows, int64_t bytes_per_row,
-                             int64_t lds, uint8_t* __restrict__ dst, int64_t ldd) {
-    // e4m3 code of each nibble value, built with the hardware conversion.
-    uint64_t lut_lo = 0, lut_hi = 0;  // nibbles 0..7 and 8..15
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        const float v = static_cast<float>(n < 8 ? n : n - 16);
-        const uint64_t code =
-            static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-        if (n < 8)
-            lut_lo |= code << (8 * n);
-        else
-            lut_hi |= code << (8 * (n - 8));
-    }
-    const int64_t per_row = bytes_per_row / 16;
-    const int64_t total = rows * per_row;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / per_row;
-        const int64_t c = (i - r * per_row) * 16;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * lds + c));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t o = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t nib = (w[q] >> (4 * (4 * h + j))) & 0xFu;
-                    const uint64_t tab = nib < 8 ? lut_lo : lut_hi;
-                    const uint32_t code = static_cast<uint32_t>(tab >> (8 * (nib & 7u))) & 0xFFu;
-                    o |= code << (8 * j);
-                }
-                out[2 * q + h] = o;
-            }
-        }
-        uint4* d = reinterpret_cast<uint4*>(dst + r * ldd + 2 * c);
-        d[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        d[1] = make_uint4(out[4], out[5], out[6], out[7]);
-    }
+// Launches k_expand over one or two operands with the same chunk count.
+template <class Conv>
+static int launch_expand(const ExpandJob* jobs, int njobs, int64_t chunks, int dev, cudaStream_t s) {
+    ExpandJobs js;
+    js.job[0] = jobs[0];
+    js.job[1] = njobs > 1 ? jobs[1] : jobs[0];
+    js.chunks = chunks;
+    int64_t rows = jobs[0].rows;
+    if (njobs > 1 && jobs[1].rows > rows) rows = jobs[1].rows;
+    const int64_t gx = (chunks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms(dev)) * 8 / njobs;
+    int64_t gy = cap / gx;
+    if (gy > rows) gy = rows;
+    if (gy > 65535) gy = 65535;
+    if (gy < 1) gy = 1;
+    if (gx > 2147483647) return QG_ERR_INVALID_ARG;
+    k_expand<Conv><<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(njobs)), 256,
+                     0, s>>>(js);
+    return map_cuda(cudaGetLastError());
 }
 
 int s4_to_e4m3(const uint8_t* src, int64_t rows, int64_t K, int64_t lds_bytes, uint8_t* dst,
                int64_t ldd, int dev, cudaStream_t s) {
-    k_s4_to_e4m3<<<conv_grid(dev, rows * K / 32), 256, 0, s>>>(src, rows, K / 2, lds_bytes, dst, ldd);
-    return map_cuda(cudaGetLastError());
+    const ExpandJob j{src, rows, lds_bytes, dst, ldd};
+    return launch_expand<S4ToE4M3>(&j, 1, K / 32, dev, s);
 }
 
 int conv_grid(int dev, int64_t work_items) {
@@ -359,9 +437,9 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, int 
     __half* A16 = static_cast<__half*>(ws);
     __half* B16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) +
                                             ((static_cast<size_t>(M) * K * 2 + 255) & ~size_t(255)));
-    k_s8_to_f16<<<conv_grid(dev, M * K / 16), 256, 0, s>>>(A, M, K, lda, A16, K);
-    k_s8_to_f16<<<conv_grid(dev, N * K / 16), 256, 0, s>>>(B, N, K, ldb, B16, K);
-    int rc = map_cuda(cudaGetLastError());
+    const ExpandJob jobs[2] = {{reinterpret_cast<const uint8_t*>(A), M, lda, reinterpret_cast<uint8_t*>(A16), K * 2},
+                               {reinterpret_cast<const uint8_t*>(B), N, ldb, reinterpret_cast<uint8_t*>(B16), K * 2}};
+    int rc = launch_expand<S8ToF16>(jobs, 2, K / 16, dev, s);
     if (rc) return rc;
     return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc,
                                                g_s8_chunk_kb, nullptr, ctl, s);
@@ -388,9 +466,8 @@ int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_byte
 
     uint8_t* A8 = static_cast<uint8_t*>(ws);
     uint8_t* B8 = static_cast<uint8_t*>(ws) + ((static_cast<size_t>(M) * K + 255) & ~size_t(255));
-    k_s4_to_e4m3<<<conv_grid(dev, M * K / 32), 256, 0, s>>>(A, M, K / 2, lda_bytes, A8, K);
-    k_s4_to_e4m3<<<conv_grid(dev, N * K / 32), 256, 0, s>>>(B, N, K / 2, ldb_bytes, B8, K);
-    int rc = map_cuda(cudaGetLastError());
+    const ExpandJob jobs[2] = {{A, M, lda_bytes, A8, K}, {B, N, ldb_bytes, B8, K}};
+    int rc = launch_expand<S4ToE4M3>(jobs, 2, K / 32, dev, s);
     if (rc) return rc;
     // Partial sums are bounded by 64*K < 2^24: one accumulation unit per tile.
     return launch_gemm<MmaKind::F8F6F4, Epi::S32>(A8, K, B8, K, M, N, K, C, ldc, 0, nullptr, ctl, s);
