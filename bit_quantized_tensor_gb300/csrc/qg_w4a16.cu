@@ -660,6 +660,187 @@ __global__ void __launch_bounds__(kD1Threads, 2)
         }
 }
 
+// ------------------------------------- decode, 9 <= M <= 16 (batched GEMV)
+//
+// The co-resident shape of k_w4a16_gemv (one CTA per SM at half its
+// resources, R <= 32 weight rows bulk-copied before the dependency wait) for
+// batches whose X (M x K fp16) does not fit next to the weights: after the
+// wait every warp reads the X fragments of its own groups straight from L2
+// (prefetching the next group's while it computes this one).  Two batch tiles
+// share every dequantized A fragment.  The nibbles become exact fp16 integers
+// (one lop3 per pair: two's-complement fix, mask and exponent of 1024; then
+// one fp16 subtract or fused multiply-add), so no group sums are needed; the
+// group scale is applied in fp32 per group.  Warp w takes groups w, w + 8, ...
+// for both m16 tiles; the partial tiles are added through shared memory.
+constexpr int kD2Warps = 8;
+constexpr int kD2Threads = 32 * kD2Warps;
+constexpr int kSiteW16D2Bulk = 305;
+constexpr int kSiteW16D2Drain = 306;
+
+struct D2Off {
+    int wrs, srs, s_off, red_off;
+};
+inline int64_t d2_bytes(int64_t M, int64_t K, int64_t R, D2Off* off) {
+    const int64_t G = K / 128;
+    const int64_t wrs = K / 2 + 64, srs = G + 1;
+    const int64_t s_off = R * wrs;
+    const int64_t red_off = s_off + ((R * srs * 4 + 15) / 16) * 16;
+    const int64_t bytes = red_off + static_cast<int64_t>(kD2Warps) * 2 * 16 * M * 4;
+    if (off) *off = D2Off{static_cast<int>(wrs), static_cast<int>(srs), static_cast<int>(s_off),
+                          static_cast<int>(red_off)};
+    return bytes;
+}
+
+template <int T>  // m16 tiles per CTA (R <= 16 T)
+__global__ void __launch_bounds__(kD2Threads, 2)
+    k_w4a16_gemv16(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
+                   const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
+                   int64_t ldy, int R, const D2Off L, const Ctl ctl) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int failed;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int G = K / kGroup;
+    const int n0 = blockIdx.x * R;
+    const int rows = min(R, N - n0);
+    uint8_t* ws = dsm;
+    float* sp = reinterpret_cast<float*>(dsm + L.s_off);
+    float* red = reinterpret_cast<float*>(dsm + L.red_off);
+    const uint32_t bar = smem_u32(&wbar);
+
+    if (threadIdx.x == 0) {
+        failed = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {  // the CTA's weight rows, one bulk copy per row
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * (K / 2));
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_copy_g2s(smem_u32(ws + r * L.wrs), Wq + static_cast<int64_t>(n0 + r) * (K / 2),
+                          static_cast<uint32_t>(K / 2), bar);
+    }
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < rows * G; i += kD2Threads) {
+        const int r = i / G, gi = i - r * G;
+        sp[r * L.srs + gi] = __half2float(__ushort_as_half(ld_nc_u16(S + static_cast<int64_t>(n0 + r) * G + gi)));
+    }
+    __syncthreads();  // scales staged
+
+    // X may be the previous kernel's output: read it only now.
+    pdl_wait_prior_grid();
+    if (!bounded_wait(bar, 0u, nullptr, ctl, kSiteW16D2Bulk)) {
+        failed = 1;
+        if (lane == 0) bounded_wait(bar, 0u, nullptr, ctl, kSiteW16D2Drain);
+    }
+    __syncthreads();
+
+    // rows past the CTA's are computed on its last row's data and never stored
+    int roff[T][2];
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt) {
+        roff[tt][0] = min(16 * tt + g, rows - 1);
+        roff[tt][1] = min(16 * tt + g + 8, rows - 1);
+    }
+    // X fragments: lane (g, t), batch tile mb holds row 8 mb + g at
+    // k = 128 g_i + 32 t + 8 i + 0..7 as (x0,x4) (x1,x5) (x2,x6) (x3,x7)
+    const bool xv0 = g < M, xv1 = 8 + g < M;
+    const __half* xr0 = X + static_cast<int64_t>(xv0 ? g : 0) * ldx + 32 * t;
+    const __half* xr1 = X + static_cast<int64_t>(xv1 ? 8 + g : 0) * ldx + 32 * t;
+    auto load_x = [&](int gi, uint4 (&xf)[2][4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            xf[0][i] = xv0 ? x_pairs(__ldg(reinterpret_cast<const uint4*>(xr0 + gi * kGroup + 8 * i)))
+                           : make_uint4(0u, 0u, 0u, 0u);
+            xf[1][i] = xv1 ? x_pairs(__ldg(reinterpret_cast<const uint4*>(xr1 + gi * kGroup + 8 * i)))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+
+    float y[T][2][4];
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt)
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[tt][mb][q] = 0.f;
+
+    uint4 xn[2][4];
+    if (warp < G) load_x(warp, xn);
+    for (int gi = warp; gi < G; gi += kD2Warps) {
+        uint4 xf[2][4];
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xf[mb][i] = xn[mb][i];
+        if (gi + kD2Warps < G) load_x(gi + kD2Warps, xn);  // next group's fragments in flight
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(ws + roff[tt][0] * L.wrs + gi * 64 + 16 * t);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(ws + roff[tt][1] * L.wrs + gi * 64 + 16 * t);
+            const float s0 = sp[roff[tt][0] * L.srs + gi], s1 = sp[roff[tt][1] * L.srs + gi];
+            float tmp[2][4];
+            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w}, wb[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t pa[4], pb[4];
+                dequant_word_fast(wa[i], pa);
+                dequant_word_fast(wb[i], pb);
+                const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+                const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb) {
+                    if (i == 0)
+                        mma_16816_c(tmp[mb], a0, xf[mb][i].x, xf[mb][i].y, 0.f, 0.f, 0.f, 0.f);
+                    else
+                        mma_16816(tmp[mb], a0, xf[mb][i].x, xf[mb][i].y);
+                    mma_16816(tmp[mb], a1, xf[mb][i].z, xf[mb][i].w);
+                }
+            }
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+                y[tt][mb][0] = fmaf(tmp[mb][0], s0, y[tt][mb][0]);
+                y[tt][mb][1] = fmaf(tmp[mb][1], s0, y[tt][mb][1]);
+                y[tt][mb][2] = fmaf(tmp[mb][2], s1, y[tt][mb][2]);
+                y[tt][mb][3] = fmaf(tmp[mb][3], s1, y[tt][mb][3]);
+            }
+        }
+    }
+
+    // partial tiles: red[warp][tile][row][m], batch rows < M only; lane (g, t)
+    // holds rows g, g + 8 and batch rows 8 mb + 2t, 8 mb + 2t + 1
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt) {
+        float* rw = red + (warp * T + tt) * 16 * M;
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int m = 8 * mb + 2 * t + j;
+                if (m < M) {
+                    rw[g * M + m] = y[tt][mb][j];
+                    rw[(g + 8) * M + m] = y[tt][mb][2 + j];
+                }
+            }
+    }
+    __syncthreads();
+    if (failed) return;
+    // output (m, r): sum of the 8 warps' partials in warp order
+    for (int o = threadIdx.x; o < rows * M; o += kD2Threads) {
+        const int r = o / M, m = o - r * M;
+        const float* pr = red + ((r >> 4) * 16 + (r & 15)) * M + m;
+        float v[kD2Warps];
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) v[w] = pr[w * T * 16 * M];
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kD2Warps; ++w) sum += v[w];
+        Y[static_cast<int64_t>(m) * ldy + n0 + r] = __float2half_rn(sum);
+    }
+}
+
 static std::atomic<int> g_w4a16_pdl{1};
 
 template <int MT, int NT>
@@ -741,6 +922,47 @@ static int launch_w4a16_gemv(int M, int N, int K, const __half* X, int64_t ldx, 
     if (R > 16)
         return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv<2>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
     return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv<1>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
+}
+
+// Rows per CTA of k_w4a16_gemv16, or 0 when it does not fit.
+static int d2_rows(int64_t M, int64_t N, int64_t K, int dev) {
+    if (M > 16) return 0;
+    const int64_t sms = num_sms(dev);
+    int64_t R = (N + sms - 1) / sms;
+    if (R > kD1MaxRows) R = kD1MaxRows;
+    while (R > 1 && static_cast<size_t>(d2_bytes(M, K, R, nullptr)) > kD1Budget) --R;
+    if (static_cast<size_t>(d2_bytes(M, K, R, nullptr)) > kD1Budget) return 0;
+    return static_cast<int>(R);
+}
+
+static int launch_w4a16_gemv16(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
+                               const __half* S, __half* Y, int64_t ldy, int R, const Ctl& ctl,
+                               cudaStream_t s) {
+    static std::atomic<int> attr_done{0};
+    if (!attr_done.load()) {
+        cudaError_t e = cudaFuncSetAttribute(k_w4a16_gemv16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kD1Budget));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_w4a16_gemv16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kD1Budget));
+        if (e != cudaSuccess) return map_cuda(e);
+        attr_done.store(1);
+    }
+    D2Off off;
+    const int64_t bytes = d2_bytes(M, K, R, &off);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + R - 1) / R));
+    cfg.blockDim = dim3(kD2Threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (R > 16)
+        return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv16<2>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
+    return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv16<1>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
 }
 }  // namespace qg
 
@@ -826,6 +1048,17 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
             const Ctl ctl = host_ctl(dev);
             if (!ctl.status) return QG_ERR_CUDA;
             return launch_w4a16_gemv(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy, R, ctl, s);
+        }
+    }
+    // Batched GEMV (X too large to stage): same co-resident shape, X from L2.
+    if (M <= 16) {
+        const int dev = current_device();
+        if (dev < 0) return QG_ERR_CUDA;
+        const int R = d2_rows(M, N, K, dev);
+        if (R > 0) {
+            const Ctl ctl = host_ctl(dev);
+            if (!ctl.status) return QG_ERR_CUDA;
+            return launch_w4a16_gemv16(static_cast<int>(M), n, k, Xh, ldx, Wq, Sh, Yh, ldy, R, ctl, s);
         }
     }
     const size_t dec_smem = dec_smem_bytes(M, K);
