@@ -53,7 +53,8 @@ def test_w4a16_4096(dev, oracle, M):
                                    (40, 72, 1024), (77, 333, 640), (130, 48, 256),
                                    (9, 4096, 11008 // 128 * 128), (2, 64, 8192),
                                    (1, 40, 16384), (12, 40, 20480), (1, 24, 20480),
-                                   (5, 33, 24576)])
+                                   (5, 33, 24576), (8, 5000, 2048), (16, 3001, 1152),
+                                   (7, 300, 4096), (13, 4864, 512)])
 def test_w4a16_shapes(dev, oracle, M, N, K):
     X, Wq, S = _operands(M, N, K, idx=M + N)
     assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), f"w4a16 {M}x{N}x{K}")
@@ -79,7 +80,7 @@ def test_w4a16_group_scales_are_per_row_and_group(dev, oracle):
     assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), "w4a16 pow2 scales")
 
 
-@pytest.mark.parametrize("M", [1, 32])
+@pytest.mark.parametrize("M", [1, 12, 32])
 @pytest.mark.parametrize("pdl", [1, 0])
 def test_w4a16_chain_reads_previous_output(dev, oracle, pdl, M):
     """Layer chain Y_i = f_i(Y_{i-1}) on one stream: with programmatic
