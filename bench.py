@@ -193,11 +193,11 @@ class Workload:
     # each op returns the number of library kernels it launched
     def s8(self):
         self.qg.qgemm_s8(self.A8, self.B8, C=self.C32, ws=self.ws8)
-        return 3
+        return 2  # operand expansion (A and B in one launch) + GEMM
 
     def s4(self):
         self.qg.qgemm_s4(self.A4, self.B4, N_SQ, C=self.C32, ws=self.ws4)
-        return 3
+        return 2
 
     def f16(self):
         self.qg.gemm_f16(self.Af, self.Bf, C=self.C16)
@@ -227,7 +227,7 @@ class Workload:
         q, s, xu = self.q_out
         self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, Vt=self.Vt, bias=self.bias,
                           Y=self.Y4, ws=self.ws_w4)
-        return 4
+        return 4  # operand expansion, two scale transposes, GEMM
 
     def flush(self):
         self.flush_buf.fill_(1)

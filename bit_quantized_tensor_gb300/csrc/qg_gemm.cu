@@ -350,10 +350,10 @@ static int launch_expand(const ExpandJob* jobs, int njobs, int64_t chunks, int d
     return map_cuda(cudaGetLastError());
 }
 
-int s4_to_e4m3(const uint8_t* src, int64_t rows, int64_t K, int64_t lds_bytes, uint8_t* dst,
-               int64_t ldd, int dev, cudaStream_t s) {
-    const ExpandJob j{src, rows, lds_bytes, dst, ldd};
-    return launch_expand<S4ToE4M3>(&j, 1, K / 32, dev, s);
+int s4_to_e4m3_pair(const uint8_t* a, int64_t a_rows, int64_t a_lds, uint8_t* a_dst, const uint8_t* b,
+                    int64_t b_rows, int64_t b_lds, uint8_t* b_dst, int64_t K, int dev, cudaStream_t s) {
+    const ExpandJob jobs[2] = {{a, a_rows, a_lds, a_dst, K}, {b, b_rows, b_lds, b_dst, K}};
+    return launch_expand<S4ToE4M3>(jobs, 2, K / 32, dev, s);
 }
 
 int conv_grid(int dev, int64_t work_items) {

@@ -35,9 +35,10 @@ int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, 
 // Grid size for the elementwise grid-stride kernels (256 threads per block).
 int conv_grid(int dev, int64_t work_items);
 
-// Packed signed 4-bit rows (K values, low nibble = even k) -> one e4m3 byte
-// per value (exact), enqueued on `s`.  K is a multiple of 32.
-int s4_to_e4m3(const uint8_t* src, int64_t rows, int64_t K, int64_t lds_bytes, uint8_t* dst,
-               int64_t ldd, int dev, cudaStream_t s);
+// Packed signed 4-bit rows (K values, low nibble = even k) of two operands
+// -> one e4m3 byte per value (exact, destination row stride K bytes), one
+// launch enqueued on `s`.  K is a multiple of 32.
+int s4_to_e4m3_pair(const uint8_t* a, int64_t a_rows, int64_t a_lds, uint8_t* a_dst, const uint8_t* b,
+                    int64_t b_rows, int64_t b_lds, uint8_t* b_dst, int64_t K, int dev, cudaStream_t s);
 
 }  // namespace qg

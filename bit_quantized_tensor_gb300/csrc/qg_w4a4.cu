@@ -483,8 +483,7 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     float* SWt = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(SXt) +
                                           up(4ull * (nblk + 1) * Mp));
 
-    int rc = s4_to_e4m3(Xq, M, K, K / 2, A8, K, dev, s);
-    if (!rc) rc = s4_to_e4m3(Wq, N, K, K / 2, B8, K, dev, s);
+    int rc = s4_to_e4m3_pair(Xq, M, K / 2, A8, Wq, N, K / 2, B8, K, dev, s);
     if (rc) return rc;
     k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
         M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), SXt);
