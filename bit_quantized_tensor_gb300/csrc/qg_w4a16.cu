@@ -436,9 +436,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 //    four lop3 (even k at bits 0-3 of each half: n * 2^-24; odd k at bits
 //    4-7: 16 n * 2^-24).  Even and odd k go to separate MMAs and
 //    accumulators (the odd one carries the factor 16), and the offset 8 is
-//    removed exactly by starting each group's even accumulator at
-//    -8 * 2^-24 * sum(x over the group), computed once per call when X is
-//    staged.  Every product is exact (an 11-bit by 4-bit product in fp32);
+//    removed by starting each group's even accumulator at
+//    -8 * 2^-24 * sum(x over the group) (the sum in fp32, fixed order),
+//    computed once per call when X is staged; the weights stay exact.  Every
+//    product is exact (an 11-bit by 4-bit product in fp32);
 //    the scale s * 2^24 (even) and s * 2^20 (odd) is applied in fp32 per
 //    group, as in the other W4A16 kernels.
 //  - X (M x K) is staged once into shared memory, already permuted into the
