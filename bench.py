@@ -233,6 +233,8 @@ class Workload:
         self.flush_buf.fill_(1)
 
 
+WORKLOAD = ("INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1/16/128 N=K=4096 g128, "
+            "W4A4 4096x8192x8192 r32 (one step = all eight ops)")
 OPS = ["s8", "s4", "f16", "w4a16", "w4a16_m16", "w4a16_m128", "w4a4_quant", "w4a4_gemm"]
 MAIN_KERNEL_OPS = {"s8", "s4", "f16", "w4a4_gemm"}  # ops with a timed tcgen05 GEMM kernel
 
@@ -376,9 +378,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-        "config": {"workload": "INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1/16/128 N=K=4096 g128, "
-                               "W4A4 4096x8192x8192 r32 (one step = all eight ops)",
-                   "N": N_SQ, "parallelism": "replicas" if world > 1 else "single GPU",
+        "config": {"workload": WORKLOAD, "N": N_SQ,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "256 MiB write before every op; every working set > L2",
                    "wall_s_timed_region": round(wall, 3)},
         "breakdown": breakdown, "roofline": roofline, "clocks": clk,
@@ -488,13 +489,14 @@ def run_reference(args, rank, world):
         last = oracle_baseline(args.cpu_seconds / max(args.steps, 1))
         vals.append(last["value"])
     wall = time.perf_counter() - t0
-    value = statistics.median(vals)
+    value = round(statistics.median(vals), 6)
     res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(wall * 1e3 / max(args.steps, 1), 1), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-           "config": {"workload": "INT8 GEMM 8192^3, bounded row sample per step (CPU oracle)",
-                      "N": N_SQ},
+           "config": {"workload": WORKLOAD, "N": N_SQ,
+                      "measured": "the headline INT8 GEMM 8192^3 only, on a bounded row sample "
+                                  "per step (see cpu_baseline.sample)"},
            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": last["cores"],
                             "kind": "oracle", "sample": last["sample"]},
            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
