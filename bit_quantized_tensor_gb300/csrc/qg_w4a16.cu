@@ -701,7 +701,9 @@ inline int64_t d2_bytes(int64_t M, int64_t K, int64_t R, D2Off* off) {
     return bytes;
 }
 
-template <int T>  // m16 tiles per CTA (R <= 16 T)
+// T: m16 tiles per CTA (R <= 16 T); GPW: groups per warp if known at
+// compile time (the group loop unrolls), else 0.
+template <int T, int GPW>
 __global__ void __launch_bounds__(kD2Threads, 2)
     k_w4a16_gemv16(int M, int N, int K, const __half* __restrict__ X, int64_t ldx,
                    const uint8_t* __restrict__ Wq, const __half* __restrict__ S, __half* __restrict__ Y,
@@ -779,7 +781,7 @@ __global__ void __launch_bounds__(kD2Threads, 2)
 
     uint4 xn[2][4];
     if (warp < G) load_x(warp, xn);
-    for (int gi = warp; gi < G; gi += kD2Warps) {
+    auto group = [&](const int gi) {
         uint4 xf[2][4];
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
@@ -817,6 +819,12 @@ __global__ void __launch_bounds__(kD2Threads, 2)
                 y[tt][mb][3] = fmaf(tmp[mb][3], s1, y[tt][mb][3]);
             }
         }
+        };
+    if constexpr (GPW > 0) {
+#pragma unroll
+        for (int j = 0; j < GPW; ++j) group(warp + j * kD2Warps);
+    } else {
+        for (int gi = warp; gi < G; gi += kD2Warps) group(gi);
     }
 
     // partial tiles: red[warp][tile][row][m], batch rows < M only; lane (g, t)
@@ -956,14 +964,23 @@ static int d2_rows(int64_t M, int64_t N, int64_t K, int dev) {
 static int launch_w4a16_gemv16(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
                                const __half* S, __half* Y, int64_t ldy, int R, const Ctl& ctl,
                                cudaStream_t s) {
+    using KernelFn = void (*)(int, int, int, const __half*, int64_t, const uint8_t*, const __half*, __half*,
+                              int64_t, int, D2Off, Ctl);
+    const int gpw = (K / kGroup) % kD2Warps == 0 ? (K / kGroup) / kD2Warps : 0;
+    KernelFn fn;
+    if (R > 16)
+        fn = gpw == 4 ? k_w4a16_gemv16<2, 4> : k_w4a16_gemv16<2, 0>;
+    else
+        fn = gpw == 4 ? k_w4a16_gemv16<1, 4> : k_w4a16_gemv16<1, 0>;
     static std::atomic<int> attr_done{0};
     if (!attr_done.load()) {
-        cudaError_t e = cudaFuncSetAttribute(k_w4a16_gemv16<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kD1Budget));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_w4a16_gemv16<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kD1Budget));
-        if (e != cudaSuccess) return map_cuda(e);
+        const KernelFn all[4] = {k_w4a16_gemv16<2, 4>, k_w4a16_gemv16<2, 0>, k_w4a16_gemv16<1, 4>,
+                                 k_w4a16_gemv16<1, 0>};
+        for (KernelFn f : all) {
+            const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kD1Budget));
+            if (e != cudaSuccess) return map_cuda(e);
+        }
         attr_done.store(1);
     }
     D2Off off;
@@ -978,9 +995,7 @@ static int launch_w4a16_gemv16(int M, int N, int K, const __half* X, int64_t ldx
     attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (R > 16)
-        return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv16<2>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
-    return map_cuda(cudaLaunchKernelEx(&cfg, k_w4a16_gemv16<1>, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
+    return map_cuda(cudaLaunchKernelEx(&cfg, fn, M, N, K, X, ldx, Wq, S, Y, ldy, R, off, ctl));
 }
 }  // namespace qg
 
