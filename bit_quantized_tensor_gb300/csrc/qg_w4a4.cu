@@ -227,19 +227,22 @@ __global__ void __launch_bounds__(kQThreads, 2)
                 x1[4 * i] = v1.x; x1[4 * i + 1] = v1.y; x1[4 * i + 2] = v1.z; x1[4 * i + 3] = v1.w;
             }
         }
-        __syncwarp();  // every lane has read the stage: refill it
-        if (lane == 0 && b + kQStages < bend) issue(b + kQStages, stage);
-        if (++stage == kQStages) {
-            stage = 0;
-            phase ^= 1u;
-        }
-
         // Per-row block absmax over the 4 lanes t of the row.
         float m0 = absmax16(x0), m1 = absmax16(x1);
         m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
         m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
         m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
         m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+        // Every lane has used its values of the stage (the absmax reads all of
+        // them): only now may the TMA overwrite it.  Refilling right after the
+        // loads, before their registers were used, raced in a ring built the
+        // same way (a slot refilled before all of its loads had read it).
+        __syncwarp();
+        if (lane == 0 && b + kQStages < bend) issue(b + kQStages, stage);
+        if (++stage == kQStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
         const __half h0 = __float2half_rn(__fdiv_rn(m0, 7.0f));
         const __half h1 = __float2half_rn(__fdiv_rn(m1, 7.0f));
         const float s0 = __half2float(h0), s1 = __half2float(h1);
