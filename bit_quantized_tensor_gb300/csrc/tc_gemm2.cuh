@@ -19,6 +19,7 @@
 //                stage s in both
 //   acc_full[b]  both CTAs; multicast commit after a unit's last MMA
 //   acc_empty[b] leader only; 8 epilogue warps of each CTA arrive remotely
+//                (relaxed: the TMEM reads are complete at tcgen05.wait::ld)
 // Every wait is bounded.  The CTAs leave only after a cluster barrier, so no
 // CTA exits while its partner may still read its shared memory or signal it.
 #pragma once
@@ -246,9 +247,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                         for (int i = 0; i < 32; ++i)
                             sum[32 * c + i] += __float2int_rn(__uint_as_float(r[i]));
                     }
+                    // The buffer's TMEM reads completed at tcgen05.wait::ld, so the
+                    // leader needs the arrival only, not a cluster-scope release.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(as.index), 0));
+                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.index), 0));
                     as.advance();
                 }
                 if (!ok) break;
@@ -277,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(as.index), 0));
+                if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.index), 0));
                 as.advance();
                 if (row < p.M)
                     store_row_f16<128>(static_cast<__half*>(p.C) + static_cast<int64_t>(row) * p.ldc +
