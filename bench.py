@@ -59,6 +59,24 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def replica_times(dist, device, total_ms: float, s8_ms: float):
+    """Replicas only: every rank runs the same step on its own GPU.  The job
+    takes as long as its slowest rank, so both the step total and the INT8
+    GEMM time are the maximum over ranks (one all_reduce); without a process
+    group they are returned as they are."""
+    if dist is None:
+        return total_ms, s8_ms
+    import torch
+    t = torch.tensor([total_ms, s8_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0].item()), float(t[1].item())
+
+
+def job_tops(ops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return world * ops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -303,11 +321,7 @@ def run_ours(args, rank, world, local_rank):
     t_op = {op: [a.elapsed_time(b) for a, b in ev[op]] for op in OPS}          # ms
     t_k = {op: [a.elapsed_time(b) for a, b in kev[op]] for op in MAIN_KERNEL_OPS}
     step_ms = [sum(t_op[op][i] for op in OPS) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms, s8_ms = replica_times(dist, dev, sum(step_ms), sum(t_op["s8"]))
 
     peaks, peak_src = load_peaks()
     bf16 = float(peaks["bf16_tflops"])
@@ -320,11 +334,7 @@ def run_ours(args, rank, world, local_rank):
     def tops(ops, ms):
         return ops / (ms * 1e-3) / 1e12
 
-    s8_tops = sum(gemm_ops for _ in t_op["s8"]) / (sum(t_op["s8"]) * 1e-3) / 1e12
-    if dist and world > 1:
-        tt = torch.tensor([sum(t_op["s8"])], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        s8_tops = world * gemm_ops * args.steps / (float(tt.item()) * 1e-3) / 1e12
+    s8_tops = job_tops(gemm_ops, args.steps, world, s8_ms)
 
     w16_call_us = med["w4a16"] * 1e3 / wl.w16_sets
     w16_gbs = wl.w16_bytes[1] / (w16_call_us * 1e-6) / 1e9
