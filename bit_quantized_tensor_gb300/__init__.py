@@ -52,9 +52,11 @@ SIGNATURES = {
     "qg_version": (_int, []),
     "qg_workspace_size": (_sz, [_int, _i64, _i64, _i64]),
     "qg_device_status": (_int, [_p]),
+    "qg_device_status_detail": (_int, [ctypes.POINTER(ctypes.c_int), _p]),
     "qg_last_cuda_error": (_int, []),
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
     "qg_selftest_wait_timeout": (_int, [ctypes.c_uint64, _p]),
+    "qg_selftest_deadlock": (_int, [_int, ctypes.c_uint64, _p]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_gemm_path": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
@@ -142,6 +144,19 @@ def _workspace(op, M, N, K, device, ws):
 
 def device_status(stream=None) -> int:
     return int(lib().qg_device_status(_stream(stream)))
+
+
+STATUS_WORDS = ("code", "site", "count", "block", "parity", "barrier")
+
+
+def device_status_detail(stream=None) -> dict:
+    """Reads and clears the device status word; returns its six fields by name
+    ("code" is QG_OK when no wait ran out since the last read)."""
+    words = (ctypes.c_int * len(STATUS_WORDS))()
+    code = int(lib().qg_device_status_detail(words, _stream(stream)))
+    if code == QG_ERR_CUDA:
+        raise QgError("qg_device_status_detail", code)
+    return dict(zip(STATUS_WORDS, (int(w) for w in words)))
 
 
 def set_timeout_ns(ns: int) -> None:

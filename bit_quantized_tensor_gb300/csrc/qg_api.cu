@@ -122,21 +122,26 @@ int qg_set_timeout_ns(uint64_t ns) {
     return QG_OK;
 }
 
-int qg_device_status(void* stream) {
+int qg_device_status_detail(int* words, void* stream) {
     const int dev = qg::current_device();
     if (dev < 0) return QG_ERR_CUDA;
     qg::Ctl c = qg::host_ctl(dev);
     if (!c.status) return QG_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return QG_ERR_CUDA;
-    int h[qg::kStatusWords] = {0, 0, 0, 0};
+    int h[qg::kStatusWords] = {};
     if (cudaMemcpy(h, c.status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return QG_ERR_CUDA;
+    if (words) {
+        for (int i = 0; i < qg::kStatusWords; ++i) words[i] = h[i];
+    }
     if (h[0] != 0) {
-        int z[qg::kStatusWords] = {0, 0, 0, 0};
+        const int z[qg::kStatusWords] = {};
         if (cudaMemcpy(c.status, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return QG_ERR_CUDA;
         return h[0];
     }
     return QG_OK;
 }
+
+int qg_device_status(void* stream) { return qg_device_status_detail(nullptr, stream); }
 
 }  // extern "C"

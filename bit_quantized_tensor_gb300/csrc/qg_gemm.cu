@@ -398,6 +398,7 @@ int qg_set_s8_chunk(int kblocks) {
 
 int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, int layout_a,
              const uint16_t* B, int64_t ldb, int layout_b, uint16_t* C, int64_t ldc, void* stream) {
+    const qg::NvtxRange nvtx_range("gemm_f16");
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return QG_ERR_INVALID_ARG;
     if (!A || !B || !C) return QG_ERR_INVALID_ARG;
@@ -418,6 +419,7 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, in
 int qgemm_s8(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, int layout_a,
              const int8_t* B, int64_t ldb, int layout_b, int32_t* C, int64_t ldc, void* ws,
              size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("qgemm_s8");
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX) return QG_ERR_INVALID_ARG;
     if (!A || !B || !C) return QG_ERR_INVALID_ARG;
     if (bad_layouts(layout_a, layout_b)) return QG_ERR_UNSUPPORTED;
@@ -448,6 +450,7 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, int 
 int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_bytes, int layout_a,
              const uint8_t* B, int64_t ldb_bytes, int layout_b, int32_t* C, int64_t ldc, void* ws,
              size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("qgemm_s4");
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX) return QG_ERR_INVALID_ARG;
     if (!A || !B || !C) return QG_ERR_INVALID_ARG;
     if (bad_layouts(layout_a, layout_b)) return QG_ERR_UNSUPPORTED;

@@ -6,14 +6,27 @@
 
 #include "qgemm.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace qg {
+
+// An NVTX range named after a C-ABI call for the object's lifetime, so each
+// call shows on a profiler's timeline (no effect unless a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Device status word layout (one per device, in qg_api.cu):
 //   [0] first error code recorded (0 = none)
-//   [1] call-site tag of that error
+//   [1] call-site tag of that error (which role of which kernel)
 //   [2] number of errors recorded
 //   [3] block index that recorded the first error
-constexpr int kStatusWords = 4;
+//   [4] phase parity the timed-out wait was waiting for
+//   [5] shared-memory address of the barrier it waited on (the ring slot)
+constexpr int kStatusWords = 6;
 
 // Backstop on bounded_wait when %globaltimer does not advance.
 constexpr uint32_t kMaxWaitIterations = 1u << 30;
@@ -25,10 +38,13 @@ struct Ctl {
     uint64_t timeout_ns;  // limit of every bounded wait
 };
 
-__device__ __forceinline__ void report_error(const Ctl& ctl, int code, int site) {
+__device__ __forceinline__ void report_error(const Ctl& ctl, int code, int site, uint32_t bar = 0,
+                                             uint32_t parity = 0) {
     if (atomicCAS(ctl.status, 0, code) == 0) {
         ctl.status[1] = site;
         ctl.status[3] = static_cast<int>(blockIdx.x);
+        ctl.status[4] = static_cast<int>(parity);
+        ctl.status[5] = static_cast<int>(bar);
     }
     atomicAdd(ctl.status + 2, 1);
 }

@@ -56,6 +56,7 @@ int scratch_address(int dev, void** out) {
 extern "C" int qgemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda,
                                 int layout_a, const int8_t* B, int64_t ldb, int layout_b,
                                 int32_t* C, int64_t ldc, void* stream) {
+    const qg::NvtxRange nvtx_range("qgemm_s8_noalloc");
     if (M < 1 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
     const size_t need = qg_workspace_size(QG_OP_S8, M, N, K);
     if (need == 0 || need > kScratchBytes) return QG_ERR_WORKSPACE;

@@ -91,7 +91,7 @@ static __device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t par
         }
     }
     if (abort_flag) *abort_flag = 1;
-    report_error(ctl, QG_ERR_TIMEOUT, site);
+    report_error(ctl, QG_ERR_TIMEOUT, site, bar, parity);
     return false;
 }
 

@@ -1056,6 +1056,7 @@ int qg_set_pdl(int enable) {
 
 int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, const uint8_t* Wq,
                const uint16_t* Wscale, int64_t group, uint16_t* Y, int64_t ldy, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a16_gemm");
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return QG_ERR_INVALID_ARG;
     if (group != kGroup) return QG_ERR_UNSUPPORTED;

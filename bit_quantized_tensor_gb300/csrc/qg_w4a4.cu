@@ -408,6 +408,7 @@ extern "C" {
 
 int w4a4_quantize(int64_t M, int64_t K, const float* X, int64_t ldx, const uint16_t* U, int64_t rank,
                   uint8_t* Xq, uint16_t* Xscale, uint16_t* XU, int64_t block, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_quantize");
     if (M < 1 || K < 1 || M > INT32_MAX || K > INT32_MAX) return QG_ERR_INVALID_ARG;
     if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;
     if (K % kW4A4Block) return QG_ERR_INVALID_ARG;
@@ -458,6 +459,7 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
               const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
               const uint16_t* V, int64_t rank, const uint16_t* bias, uint16_t* Y, int64_t ldy,
               void* ws, size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_gemm");
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return QG_ERR_INVALID_ARG;
     if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;

@@ -79,6 +79,13 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K);
  * call gave up on a bounded wait.  A failed CUDA call returns QG_ERR_CUDA. */
 int qg_device_status(void *stream);
 
+/* As qg_device_status, and also copies the whole status word into words[6]
+ * (words may be NULL): {error code, call-site tag of the role that gave up,
+ * number of errors recorded, block index, phase parity that wait expected,
+ * shared-memory address of the barrier it waited on}.  The tag and the last
+ * two words say which role, which ring slot and which phase stalled. */
+int qg_device_status_detail(int *words, void *stream);
+
 /* Diagnostics: the code of the most recent failed CUDA call behind a
  * QG_ERR_CUDA (a cudaError_t, or minus a CUresult for a driver call such as
  * the tensor-map encoder), 0 if none; reading it clears it. */
@@ -96,6 +103,21 @@ int qg_set_timeout_ns(uint64_t ns);
  * reports QG_ERR_TIMEOUT once and clears it.  Nothing faults or traps, and the
  * context stays usable.  QG_ERR_INVALID_ARG for a limit out of range. */
 int qg_selftest_wait_timeout(uint64_t limit_ns, void *stream);
+
+/* Self-test of the three deadlock patterns of a hand-built asynchronous
+ * pipeline ("Warp-Specialized Kernel Implementation for W4A4 MatMul ...",
+ * section 3), staged in one CTA with every wait bounded by limit_ns
+ * (1 .. 1e9):
+ *   1 = incomplete arrival count (a barrier expecting two producers gets one;
+ *       site tag 901),
+ *   2 = phase mismatch (the consumer waits on the wrong parity, 1, of a
+ *       barrier whose phase 0 has completed; tag 902),
+ *   3 = dependency cycle (two roles each wait for the other's arrival first;
+ *       tag 903 or 904, whichever gives up first).
+ * Each ends in QG_ERR_TIMEOUT in the device status word, read back by
+ * qg_device_status_detail; nothing faults or hangs and the context stays
+ * usable.  QG_ERR_INVALID_ARG for another pattern or a limit out of range. */
+int qg_selftest_deadlock(int pattern, uint64_t limit_ns, void *stream);
 
 /* Testing hook: K-chunk length of qgemm_s8, in blocks of 64 (1..16, default
  * 16 = 1024).  Every chunk's fp32 partial sums stay within 2^24 for any
