@@ -41,6 +41,12 @@ class QgError(RuntimeError):
         self.code = code
 
 
+class KernelBudgetC(ctypes.Structure):
+    """qg_kernel_budget of the C ABI."""
+    _fields_ = [("kernel", ctypes.c_char_p), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("tmem_cols", ctypes.c_int), ("cluster", ctypes.c_int), ("min_ctas_per_sm", ctypes.c_int)]
+
+
 _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -57,6 +63,9 @@ SIGNATURES = {
     "qg_set_timeout_ns": (_int, [ctypes.c_uint64]),
     "qg_selftest_wait_timeout": (_int, [ctypes.c_uint64, _p]),
     "qg_selftest_deadlock": (_int, [_int, ctypes.c_uint64, _p]),
+    "qg_kernel_budget_count": (_int, []),
+    "qg_kernel_budget_get": (_int, [_int, ctypes.POINTER(KernelBudgetC)]),
+    "qg_kernel_budget_measure": (_int, [_int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_gemm_path": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
@@ -157,6 +166,27 @@ def device_status_detail(stream=None) -> dict:
     if code == QG_ERR_CUDA:
         raise QgError("qg_device_status_detail", code)
     return dict(zip(STATUS_WORDS, (int(w) for w in words)))
+
+
+def kernel_budgets(measure: bool = False) -> list:
+    """The library's kernel budget table, one dict per kernel instance.  With
+    measure=True (needs a device) each entry also gets the compiled kernel's
+    registers per thread, static shared memory and the CTAs per SM the
+    device's occupancy calculator gives at the entry's launch shape."""
+    L = lib()
+    out = []
+    for i in range(int(L.qg_kernel_budget_count())):
+        b = KernelBudgetC()
+        _check("qg_kernel_budget_get", L.qg_kernel_budget_get(i, ctypes.byref(b)))
+        e = {name: getattr(b, name) for name, _ in KernelBudgetC._fields_}
+        e["kernel"] = b.kernel.decode()
+        if measure:
+            regs, ssm, ctas = _int(), _int(), _int()
+            _check("qg_kernel_budget_measure",
+                   L.qg_kernel_budget_measure(i, ctypes.byref(regs), ctypes.byref(ssm), ctypes.byref(ctas)))
+            e.update(regs_per_thread=regs.value, static_smem_bytes=ssm.value, ctas_per_sm=ctas.value)
+        out.append(e)
+    return out
 
 
 def set_timeout_ns(ns: int) -> None:

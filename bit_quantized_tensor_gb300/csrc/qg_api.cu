@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "qg_internal.h"
 
@@ -28,9 +29,25 @@ uint64_t timeout_from_env() {
     return qg::kDefaultTimeoutNs;
 }
 
+std::vector<qg::KernelBudget>& budgets() {
+    static std::vector<qg::KernelBudget> v;
+    return v;
+}
+
+std::mutex& budgets_mutex() {
+    static std::mutex m;
+    return m;
+}
+
 }  // namespace
 
 namespace qg {
+
+int register_kernel_budget(const KernelBudget& b) {
+    std::lock_guard<std::mutex> g(budgets_mutex());
+    budgets().push_back(b);
+    return static_cast<int>(budgets().size()) - 1;
+}
 
 int record_cuda_error(int code) {
     g_last_cuda_error.store(code);
@@ -143,5 +160,50 @@ int qg_device_status_detail(int* words, void* stream) {
 }
 
 int qg_device_status(void* stream) { return qg_device_status_detail(nullptr, stream); }
+
+int qg_kernel_budget_count(void) {
+    std::lock_guard<std::mutex> g(budgets_mutex());
+    return static_cast<int>(budgets().size());
+}
+
+int qg_kernel_budget_get(int index, qg_kernel_budget* out) {
+    if (!out) return QG_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(budgets_mutex());
+    if (index < 0 || index >= static_cast<int>(budgets().size())) return QG_ERR_INVALID_ARG;
+    const qg::KernelBudget& b = budgets()[static_cast<size_t>(index)];
+    out->kernel = b.name;
+    out->threads = b.threads;
+    out->smem_bytes = b.smem_bytes;
+    out->tmem_cols = b.tmem_cols;
+    out->cluster = b.cluster;
+    out->min_ctas_per_sm = b.min_ctas_per_sm;
+    return QG_OK;
+}
+
+int qg_kernel_budget_measure(int index, int* regs_per_thread, int* static_smem_bytes,
+                             int* ctas_per_sm) {
+    if (!regs_per_thread || !static_smem_bytes || !ctas_per_sm) return QG_ERR_INVALID_ARG;
+    qg::KernelBudget b;
+    {
+        std::lock_guard<std::mutex> g(budgets_mutex());
+        if (index < 0 || index >= static_cast<int>(budgets().size())) return QG_ERR_INVALID_ARG;
+        b = budgets()[static_cast<size_t>(index)];
+    }
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, b.func);
+    if (e != cudaSuccess) return qg::map_cuda(e);
+    *regs_per_thread = fa.numRegs;
+    *static_smem_bytes = static_cast<int>(fa.sharedSizeBytes);
+    if (b.smem_bytes > 0) {
+        e = cudaFuncSetAttribute(b.func, cudaFuncAttributeMaxDynamicSharedMemorySize, b.smem_bytes);
+        if (e != cudaSuccess) return qg::map_cuda(e);
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, b.func, b.threads,
+                                                      static_cast<size_t>(b.smem_bytes));
+    if (e != cudaSuccess) return qg::map_cuda(e);
+    *ctas_per_sm = n;
+    return QG_OK;
+}
 
 }  // extern "C"

@@ -369,6 +369,32 @@ int conv_grid(int dev, int64_t work_items) {
 // every fp32 partial sum within 2^24.  Adjustable for tests.
 static int g_s8_chunk_kb = 16;
 
+// Resource budgets of the instances launched above.
+#define QG_TC_BUDGET(CFG, NAME, CLUSTER)                                                      \
+    QG_KERNEL_BUDGET(NAME, reinterpret_cast<const void*>(CFG), CFG##_Cfg::THREADS,              \
+                     CFG##_Cfg::SMEM_BYTES, CFG##_Cfg::TMEM_COLS, CLUSTER, 1)
+using TcS8_Cfg = TcGemmCfg<MmaKind::F16, Epi::S32>;
+using TcS4_Cfg = TcGemmCfg<MmaKind::F8F6F4, Epi::S32>;
+using TcF16_Cfg = TcGemmCfg<MmaKind::F16, Epi::F16>;
+using Tc2S8_Cfg = Tc2Cfg<MmaKind::F16, Epi::S32>;
+using Tc2S4_Cfg = Tc2Cfg<MmaKind::F8F6F4, Epi::S32>;
+using Tc2F16_Cfg = Tc2Cfg<MmaKind::F16, Epi::F16>;
+static constexpr auto TcS8 = tc_gemm_kernel<TcS8_Cfg>;
+static constexpr auto TcS4 = tc_gemm_kernel<TcS4_Cfg>;
+static constexpr auto TcF16 = tc_gemm_kernel<TcF16_Cfg>;
+static constexpr auto Tc2S8 = tc_gemm2_kernel<Tc2S8_Cfg>;
+static constexpr auto Tc2S4 = tc_gemm2_kernel<Tc2S4_Cfg>;
+static constexpr auto Tc2F16 = tc_gemm2_kernel<Tc2F16_Cfg>;
+QG_TC_BUDGET(TcS8, "tc_gemm_kernel<F16,S32>", 1);
+QG_TC_BUDGET(TcS4, "tc_gemm_kernel<F8F6F4,S32>", 1);
+QG_TC_BUDGET(TcF16, "tc_gemm_kernel<F16,F16>", 1);
+QG_TC_BUDGET(Tc2S8, "tc_gemm2_kernel<F16,S32>", 2);
+QG_TC_BUDGET(Tc2S4, "tc_gemm2_kernel<F8F6F4,S32>", 2);
+QG_TC_BUDGET(Tc2F16, "tc_gemm2_kernel<F16,F16>", 2);
+#undef QG_TC_BUDGET
+QG_KERNEL_BUDGET("k_expand<S8ToF16>", reinterpret_cast<const void*>(k_expand<S8ToF16>), 256, 0, 0, 1, 1);
+QG_KERNEL_BUDGET("k_expand<S4ToE4M3>", reinterpret_cast<const void*>(k_expand<S4ToE4M3>), 256, 0, 0, 1, 1);
+
 }  // namespace qg
 
 using namespace qg;

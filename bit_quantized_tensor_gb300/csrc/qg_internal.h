@@ -49,6 +49,29 @@ __device__ __forceinline__ void report_error(const Ctl& ctl, int code, int site,
     atomicAdd(ctl.status + 2, 1);
 }
 
+// Resource budget of one kernel instance: what a CTA of it asks of an SM and
+// how many CTAs of it the design counts on finding resident on one SM.  Each
+// translation unit registers the instances it launches (QG_KERNEL_BUDGET) at
+// load time; the C ABI lists them (qg_kernel_budget_*), so that tests can
+// check the accounting on the host and the real residency (registers
+// included) on a device.
+struct KernelBudget {
+    const char* name;     // kernel with its template arguments
+    const void* func;     // host stub, for occupancy queries
+    int threads;          // threads per CTA
+    int smem_bytes;       // largest dynamic shared memory a launch requests
+    int tmem_cols;        // tensor-memory columns each CTA allocates (0 = none)
+    int cluster;          // CTAs per cluster
+    int min_ctas_per_sm;  // CTAs of this kernel the design needs resident per SM
+};
+int register_kernel_budget(const KernelBudget& b);
+
+#define QG_BUDGET_CAT2(a, b) a##b
+#define QG_BUDGET_CAT(a, b) QG_BUDGET_CAT2(a, b)
+#define QG_KERNEL_BUDGET(...)                                       \
+    static const int QG_BUDGET_CAT(qg_kernel_budget_, __COUNTER__) = \
+        ::qg::register_kernel_budget(::qg::KernelBudget{__VA_ARGS__})
+
 // Host helpers (qg_api.cu).
 Ctl host_ctl(int device);  // status pointer of `device` + current timeout
 int num_sms(int device);

@@ -1043,6 +1043,30 @@ static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M
     return map_cuda(cudaLaunchKernelEx(&cfg, w4a16_tc_kernel, tmX, tmW, p));
 }
 
+// Resource budgets of the instances launched above.  The GEMV kernels count
+// on two CTAs per SM (the next call's CTAs start while this call's run).
+#define QG_W16_BUDGET(FN, NAME, THREADS, SMEM, MIN_CTAS) \
+    QG_KERNEL_BUDGET(NAME, reinterpret_cast<const void*>(FN), THREADS, SMEM, 0, 1, MIN_CTAS)
+QG_W16_BUDGET((k_w4a16<1, 2>), "k_w4a16<1,2>", kW16Threads, 0, 1);
+QG_W16_BUDGET((k_w4a16<2, 4>), "k_w4a16<2,4>", kW16Threads, 0, 1);
+QG_W16_BUDGET((k_w4a16<4, 8>), "k_w4a16<4,8>", kW16Threads, 0, 1);
+QG_W16_BUDGET((k_w4a16<8, 8>), "k_w4a16<8,8>", kW16Threads, 0, 1);
+QG_W16_BUDGET((k_w4a16_dec<1>), "k_w4a16_dec<1>", kDecThreads, static_cast<int>(kDecMaxSmem), 1);
+QG_W16_BUDGET((k_w4a16_dec<2>), "k_w4a16_dec<2>", kDecThreads, static_cast<int>(kDecMaxSmem), 1);
+QG_W16_BUDGET((k_w4a16_gemv<2, 4>), "k_w4a16_gemv<2,4>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv<2, 8>), "k_w4a16_gemv<2,8>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv<2, 0>), "k_w4a16_gemv<2,0>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv<1, 2>), "k_w4a16_gemv<1,2>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv<1, 4>), "k_w4a16_gemv<1,4>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv<1, 0>), "k_w4a16_gemv<1,0>", kD1Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv16<2, 4>), "k_w4a16_gemv16<2,4>", kD2Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv16<2, 0>), "k_w4a16_gemv16<2,0>", kD2Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv16<1, 4>), "k_w4a16_gemv16<1,4>", kD2Threads, static_cast<int>(kD1Budget), 2);
+QG_W16_BUDGET((k_w4a16_gemv16<1, 0>), "k_w4a16_gemv16<1,0>", kD2Threads, static_cast<int>(kD1Budget), 2);
+#undef QG_W16_BUDGET
+QG_KERNEL_BUDGET("w4a16_tc_kernel", reinterpret_cast<const void*>(w4a16_tc_kernel), W16TcCfg::THREADS,
+                 W16TcCfg::SMEM_BYTES, W16TcCfg::TMEM_COLS, W16TcCfg::KSPLIT, 1);
+
 }  // namespace qg
 
 using namespace qg;

@@ -400,6 +400,18 @@ static int launch_w4a4(const uint8_t* A8, const uint8_t* B8, const float* SXt, c
     return rc;
 }
 
+// Resource budgets of the instances launched above.  The quantizer counts on
+// two CTAs per SM.
+QG_KERNEL_BUDGET("k_w4a4_quantize<true>", reinterpret_cast<const void*>(k_w4a4_quantize<true>), kQThreads,
+                 kQSmemBytes, 0, 1, 2);
+QG_KERNEL_BUDGET("k_w4a4_quantize<false>", reinterpret_cast<const void*>(k_w4a4_quantize<false>), kQThreads,
+                 kQSmemBytes, 0, 1, 2);
+QG_KERNEL_BUDGET("k_scales_transposed", reinterpret_cast<const void*>(k_scales_transposed), 256, 0, 0, 1, 1);
+QG_KERNEL_BUDGET("w4a4_gemm_kernel", reinterpret_cast<const void*>(w4a4_gemm_kernel), W4A4Cfg::THREADS,
+                 W4A4Cfg::SMEM_BYTES, W4A4Cfg::TMEM_COLS, 1, 1);
+QG_KERNEL_BUDGET("w4a4_gemm2_kernel", reinterpret_cast<const void*>(w4a4_gemm2_kernel), W4A4PairCfg::THREADS,
+                 W4A4PairCfg::SMEM_BYTES, W4A4PairCfg::TMEM_COLS, 2, 1);
+
 }  // namespace qg
 
 using namespace qg;

@@ -96,6 +96,36 @@ int qg_last_cuda_error(void);
  * the default. */
 int qg_set_timeout_ns(uint64_t ns);
 
+/* Resource budget of one kernel instance of the library: what one CTA asks
+ * of an SM and how many CTAs of it the design relies on finding resident per
+ * SM (two for the W4A16 GEMV kernels and the W4A4 quantizer, whose next call
+ * starts while the current one runs; one for the tensor-memory kernels, which
+ * must never share an SM with a second CTA of themselves, since the tensor
+ * memory of an SM is 512 columns).  `kernel` is a static string. */
+typedef struct {
+    const char *kernel;   /* kernel name with its template arguments */
+    int threads;          /* threads per CTA */
+    int smem_bytes;       /* largest dynamic shared memory a launch requests */
+    int tmem_cols;        /* tensor-memory columns each CTA allocates (0 = none) */
+    int cluster;          /* CTAs per thread-block cluster */
+    int min_ctas_per_sm;  /* CTAs the design needs resident on one SM */
+} qg_kernel_budget;
+
+/* Number of kernel instances in the budget table (host only, no device). */
+int qg_kernel_budget_count(void);
+
+/* Copies entry `index` (0 .. count-1) into *out; host only.
+ * QG_ERR_INVALID_ARG for an index out of range or a NULL out. */
+int qg_kernel_budget_get(int index, qg_kernel_budget *out);
+
+/* Needs a device: the compiled kernel's registers per thread and static
+ * shared memory, and the CTAs per SM that the device would keep resident at
+ * the entry's threads and dynamic shared memory (the runtime's occupancy
+ * calculator; it raises the kernel's dynamic shared-memory limit to the
+ * entry's size first, as the launcher does).  QG_ERR_CUDA without a device. */
+int qg_kernel_budget_measure(int index, int *regs_per_thread, int *static_smem_bytes,
+                             int *ctas_per_sm);
+
 /* Self-test of the failure path (no counterpart on the pages): enqueues one
  * CTA that waits on an mbarrier nothing arrives on, with a limit of limit_ns
  * (1 .. 1e9).  The wait runs out, the kernel records QG_ERR_TIMEOUT (call-site
