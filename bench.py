@@ -49,6 +49,37 @@ FP8_RATIO, FP4_RATIO = 2.0, 6.0
 # measured for the current kernel (the capture command is in the profiles).
 S8_MAIN_DRAM_BYTES = 1086626560 + 250137600
 
+# Performance-regression floors: (breakdown entry, key) -> lowest accepted
+# fraction of its peak, about 15% under what GB300 measures.  The line
+# reports which floors were missed; --check-floors also exits 1 on a miss.
+FLOORS = {
+    ("int8_gemm_8192", "frac_of_f16_peak"): 0.69,
+    ("int4_gemm_8192", "frac_of_fp8_peak"): 0.64,
+    ("fp16_gemm_8192", "frac_of_f16_peak"): 0.77,
+    ("w4a16_m1_4096", "frac_of_hbm"): 0.32,
+    ("w4a16_m16_4096", "frac_of_hbm"): 0.18,
+    ("w4a16_m128_4096", "frac_of_hbm"): 0.10,
+    ("w4a4_4096x8192x8192_r32", "frac_of_f16_peak"): 0.31,
+}
+
+# One-knob ablations (--ablate NAME): the library setter, the values tried
+# (the default first) and the ops whose speed the knob can change.
+ABLATIONS = {
+    "gemm_path": ("qg_set_gemm_path", (0, 1, 2), ("s8", "s4", "f16", "w4a4_gemm")),
+    "pdl": ("qg_set_pdl", (1, 0), ("w4a16", "w4a16_m16", "w4a16_m128")),
+    "s8_chunk": ("qg_set_s8_chunk", (16, 8, 4), ("s8",)),
+}
+
+
+def check_floors(breakdown: dict, floors: dict = FLOORS) -> dict:
+    """Compares the breakdown's roofline fractions with the floors."""
+    failed = []
+    for (entry, key), floor in floors.items():
+        got = breakdown.get(entry, {}).get(key)
+        if got is None or got < floor:
+            failed.append({"op": entry, "key": key, "value": got, "floor": floor})
+    return {"ok": not failed, "failed": failed}
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -199,6 +230,11 @@ class Workload:
         torch.cuda.synchronize()
         # The decode rotation is replayed as one CUDA graph (programmatic
         # dependent launch edges are kept), so host launch cost is not timed.
+        self.capture_w16()
+
+    def capture_w16(self):
+        """(Re)captures the W4A16 rotations, e.g. after the PDL switch changed."""
+        torch = self.torch
         self.w16_graph = {}
         for m in W16_MS:
             self._w4a16_calls(m)
@@ -393,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "256 MiB write before every op; every working set > L2",
                    "wall_s_timed_region": round(wall, 3)},
         "breakdown": breakdown, "roofline": roofline, "clocks": clk,
-        "gpu_launches": launches,
+        "gpu_launches": launches, "floors": check_floors(breakdown),
     }
     if rank == 0 and args.e2e:
         result["e2e"] = measure_e2e(wl, args)
@@ -403,6 +439,46 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result))
+    return result
+
+
+def run_ablation(args, local_rank):
+    """Times the ops a knob can change at each of its values (same inputs,
+    flushes and events as the main step) and prints one JSON line per value:
+    an ablation of one parameter at a time, not a bench line."""
+    import torch
+    import bit_quantized_tensor_gb300 as qg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    qg.lib()
+    wl = Workload(dev)
+    stream = torch.cuda.current_stream()
+    setter, values, ops = ABLATIONS[args.ablate]
+    try:
+        for v in values:
+            assert getattr(qg.lib(), setter)(v) == qg.QG_OK
+            if args.ablate == "pdl":
+                wl.capture_w16()
+            ev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.steps)] for op in ops}
+            for i in range(-max(args.warmup, 0), args.steps):
+                for op in ops:
+                    wl.flush()
+                    if i >= 0:
+                        ev[op][i][0].record(stream)
+                    getattr(wl, op)()
+                    if i >= 0:
+                        ev[op][i][1].record(stream)
+            torch.cuda.synchronize()
+            assert qg.device_status() == qg.QG_OK
+            med = {op: statistics.median(a.elapsed_time(b) for a, b in ev[op]) for op in ops}
+            print(json.dumps({"ablate": args.ablate, "setting": v, "default": v == values[0],
+                              "steps": args.steps, "op_ms_median": {op: round(t, 4) for op, t in med.items()}}))
+    finally:
+        getattr(qg.lib(), setter)(values[0])
+        if args.ablate == "pdl":
+            wl.capture_w16()
 
 
 def measure_e2e(wl, args, chunks: int = 8):
@@ -524,14 +600,24 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU seconds of the oracle baseline sample")
+    ap.add_argument("--check-floors", action="store_true",
+                    help="exit 1 when an op falls under its regression floor")
+    ap.add_argument("--ablate", choices=sorted(ABLATIONS),
+                    help="time the ops one knob changes at each of its values instead (one line per value)")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()
     if args.impl == "reference":
         run_reference(args, rank, world)
-    else:
-        import __graft_entry__
-        __graft_entry__.build_library()
-        run_ours(args, rank, world, local_rank)
+        return
+    import __graft_entry__
+    __graft_entry__.build_library()
+    if args.ablate:
+        if rank == 0:
+            run_ablation(args, local_rank)
+        return
+    result = run_ours(args, rank, world, local_rank)
+    if args.check_floors and rank == 0 and not result["floors"]["ok"]:
+        raise SystemExit(1)
 
 
 if __name__ == "__main__":
