@@ -344,7 +344,7 @@ __global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
 namespace qg {
 
 // Tensor maps and launch of one of the two W4A4 GEMM kernels (one CTA per
-// 128 x 192 tile, or CTA pairs per 256 x 128 tile).
+// 128 x 192 tile, or CTA pairs per 256 x 192 tile).
 template <class Cfg, bool PAIR>
 static int launch_w4a4(const uint8_t* A8, const uint8_t* B8, const float* SXt, const float* SWt,
                        const uint16_t* XU, const uint16_t* V, int64_t M, int64_t N, int64_t K,
