@@ -481,48 +481,30 @@ def run_ablation(args, local_rank):
             wl.capture_w16()
 
 
-def measure_e2e(wl, args, chunks: int = 8):
-    """qgemm_s8 through the public binding with host buffers: pinned H2D of A
-    and B, the GEMM, D2H of C, all inside the timed region.  The GEMM is
-    issued as `chunks` row slices of A and C (each a full qgemm_s8 call, so
-    B is converted once per slice), and three streams overlap the copies of
-    one slice with the arithmetic of its neighbours."""
+def measure_e2e(wl, args):
+    """The INT8 GEMM end to end through the public binding: qgemm_s8_host
+    with A and B in page-locked host memory and C written back to page-locked
+    host memory.  Every step's host-to-device copies of A and B and the
+    device-to-host copy of C happen inside the call (overlapped with the
+    conversion and GEMM of finished pieces on the library's own streams) and
+    inside the timed region, which runs from the call to the stream
+    synchronize on the host clock."""
     import torch
-    n = N_SQ
+    qg, n = wl.qg, N_SQ
     hA = wl.A8.cpu().pin_memory()
     hB = wl.B8.cpu().pin_memory()
     hC = torch.empty((n, n), dtype=torch.int32).pin_memory()
-    dA, dB = torch.empty_like(wl.A8), torch.empty_like(wl.B8)
-    rows = n // chunks
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_b = torch.cuda.Event()
-    ev_a = [torch.cuda.Event() for _ in range(chunks)]
-    ev_c = [torch.cuda.Event() for _ in range(chunks)]
+    ws = torch.empty(qg.workspace_size(qg.QG_OP_S8_HOST, n, n, n), dtype=torch.uint8, device=wl.dev)
+    stream = torch.cuda.current_stream()
 
     def once():
-        with torch.cuda.stream(s_in):
-            dB.copy_(hB, non_blocking=True)
-            ev_b.record(s_in)
-            for i in range(chunks):
-                sl = slice(i * rows, (i + 1) * rows)
-                dA[sl].copy_(hA[sl], non_blocking=True)
-                ev_a[i].record(s_in)
-        s_comp.wait_event(ev_b)
-        for i in range(chunks):
-            sl = slice(i * rows, (i + 1) * rows)
-            s_comp.wait_event(ev_a[i])
-            wl.qg.qgemm_s8(dA[sl], dB, C=wl.C32[sl], ws=wl.ws8, stream=s_comp)
-            ev_c[i].record(s_comp)
-        with torch.cuda.stream(s_out):
-            for i in range(chunks):
-                sl = slice(i * rows, (i + 1) * rows)
-                s_out.wait_event(ev_c[i])
-                hC[sl].copy_(wl.C32[sl], non_blocking=True)
-        s_out.synchronize()
+        qg.qgemm_s8_host(hA, hB, C=hC, ws=ws, stream=stream)
+        stream.synchronize()
 
     for _ in range(2):
         once()
-    assert torch.equal(hC[:4], wl.C32[:4].cpu()), "end-to-end result differs from the device result"
+    head = qg.qgemm_s8(wl.A8[:4], wl.B8).cpu()
+    assert torch.equal(hC[:4], head), "end-to-end result differs from the device result"
     ts = []
     for _ in range(max(3, args.steps)):
         t0 = time.perf_counter()
@@ -531,8 +513,8 @@ def measure_e2e(wl, args, chunks: int = 8):
     t = statistics.median(ts)
     return {"value": round(2.0 * n ** 3 / t / 1e12, 1), "unit": "TOPS",
             "h2d_bytes_per_step": 2 * n * n, "d2h_bytes_per_step": 4 * n * n,
-            "op": f"qgemm_s8 8192^3 with pinned host buffers, {chunks} row slices; H2D, GEMM and "
-                  "D2H overlapped on three streams"}
+            "op": "qgemm_s8_host 8192^3 from and to pinned host memory (8 x 2 pieces: copy-in, "
+                  "conversion + GEMM and copy-out overlapped on the library's three streams)"}
 
 
 def oracle_baseline(seconds: float, rows: int | None = None):

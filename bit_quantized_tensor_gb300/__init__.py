@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED",
                 3: "QG_ERR_MISALIGNED", 4: "QG_ERR_WORKSPACE", 5: "QG_ERR_CUDA",
                 6: "QG_ERR_TIMEOUT"}
 QG_ROW_MAJOR, QG_COL_MAJOR = 0, 1
-QG_OP_S8, QG_OP_S4, QG_OP_F16, QG_OP_W4A16, QG_OP_W4A4 = range(5)
+QG_OP_S8, QG_OP_S4, QG_OP_F16, QG_OP_W4A16, QG_OP_W4A4, QG_OP_S8_HOST = range(6)
 
 
 class QgError(RuntimeError):
@@ -72,6 +72,7 @@ SIGNATURES = {
     "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "qgemm_s8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),
+    "qgemm_s8_host": (_int, [_i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _sz, _p]),
     "qgemm_s4": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "gemm_f16": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),
     "w4a16_gemm": (_int, [_i64, _i64, _i64, _p, _i64, _p, _p, _i64, _p, _i64, _p]),
@@ -209,6 +210,40 @@ def qgemm_s8(A, B, C=None, ws=None, stream=None):
                                       B.data_ptr(), B.stride(0), QG_COL_MAJOR,
                                       C.data_ptr(), C.stride(0), ws.data_ptr(), wsb,
                                       _stream(stream)))
+    return C
+
+
+def _host(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU (host) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 2 or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+
+
+def qgemm_s8_host(A, B, C=None, ws=None, stream=None):
+    """qgemm_s8 with A (M x K int8), B (N x K int8) and C (M x N int32) in host
+    memory; the copies both ways run inside the call, overlapped with the
+    arithmetic.  Use page-locked tensors (``pin_memory()``) for full link
+    speed.  The call is asynchronous: C is complete once ``stream`` (default:
+    the current stream) has been synchronized.  ``ws`` is a device workspace
+    (allocated on the current device when None)."""
+    torch = _torch()
+    _host(A, torch.int8, "A")
+    _host(B, torch.int8, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("B must be N x K (K-major)")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.int32, pin_memory=A.is_pinned())
+    _host(C, torch.int32, "C")
+    ws, wsb = _workspace(QG_OP_S8_HOST, M, N, K, torch.device("cuda", torch.cuda.current_device()), ws)
+    _check("qgemm_s8_host", lib().qgemm_s8_host(M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                                                C.data_ptr(), C.stride(0), ws.data_ptr(), wsb,
+                                                _stream(stream)))
     return C
 
 

@@ -121,6 +121,8 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
             return round_up256(2 * m * k) + round_up256(2 * n * k);
         case QG_OP_S4:  // e4m3 copies of both operands (exact for int4 values)
             return round_up256(m * k) + round_up256(n * k);
+        case QG_OP_S8_HOST:  // device copies of A, B, C and fp16 forms of A, B
+            return qg::s8_host_workspace(M, N, K);
         case QG_OP_W4A4: {  // e4m3 operands, transposed fp32 scale tables
             const size_t nblk = k / 64 + 1;
             const size_t mp = (m + 3) & ~static_cast<size_t>(3), np = (n + 3) & ~static_cast<size_t>(3);

@@ -350,6 +350,13 @@ static int launch_expand(const ExpandJob* jobs, int njobs, int64_t chunks, int d
     return map_cuda(cudaGetLastError());
 }
 
+int s8_to_f16_rows(const int8_t* src, int64_t rows, int64_t lds, __half* dst, int64_t K, int dev,
+                   cudaStream_t s) {
+    const ExpandJob job = {reinterpret_cast<const uint8_t*>(src), rows, lds, reinterpret_cast<uint8_t*>(dst),
+                           K * 2};
+    return launch_expand<S8ToF16>(&job, 1, K / 16, dev, s);
+}
+
 int s4_to_e4m3_pair(const uint8_t* a, int64_t a_rows, int64_t a_lds, uint8_t* a_dst, const uint8_t* b,
                     int64_t b_rows, int64_t b_lds, uint8_t* b_dst, int64_t K, int dev, cudaStream_t s) {
     const ExpandJob jobs[2] = {{a, a_rows, a_lds, a_dst, K}, {b, b_rows, b_lds, b_dst, K}};
@@ -368,6 +375,12 @@ int conv_grid(int dev, int64_t work_items) {
 // Chunk length (in k-blocks of 64) of the exact int8 path; <= 16 keeps
 // every fp32 partial sum within 2^24.  Adjustable for tests.
 static int g_s8_chunk_kb = 16;
+
+int run_gemm_s8_converted(const __half* A16, const __half* B16, int64_t M, int64_t N, int64_t K, int32_t* C,
+                          int64_t ldc, const Ctl& ctl, cudaStream_t stream) {
+    return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc, g_s8_chunk_kb, nullptr,
+                                               ctl, stream);
+}
 
 // Resource budgets of the instances launched above.
 #define QG_TC_BUDGET(CFG, NAME, CLUSTER)                                                      \

@@ -32,6 +32,18 @@ int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, 
                     int64_t K, __half* C, int64_t ldc, const __half* bias, const Ctl& ctl,
                     cudaStream_t stream);
 
+// int8 rows (K values, source row stride lds bytes) -> fp16 rows of K values
+// (exact), destination rows K apart; one launch enqueued on `s`.  K is a
+// multiple of 16.
+int s8_to_f16_rows(const int8_t* src, int64_t rows, int64_t lds, __half* dst, int64_t K, int dev,
+                   cudaStream_t s);
+
+// The exact INT8 GEMM on operands already converted to fp16 (A16: M x K,
+// B16: N x K, both with row stride K): C = A . B^T in int32 (ldc elements),
+// with the K-chunk length qg_set_s8_chunk selects.
+int run_gemm_s8_converted(const __half* A16, const __half* B16, int64_t M, int64_t N, int64_t K, int32_t* C,
+                          int64_t ldc, const Ctl& ctl, cudaStream_t stream);
+
 // Grid size for the elementwise grid-stride kernels (256 threads per block).
 int conv_grid(int dev, int64_t work_items);
 

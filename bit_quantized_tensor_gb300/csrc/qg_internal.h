@@ -72,6 +72,9 @@ int register_kernel_budget(const KernelBudget& b);
     static const int QG_BUDGET_CAT(qg_kernel_budget_, __COUNTER__) = \
         ::qg::register_kernel_budget(::qg::KernelBudget{__VA_ARGS__})
 
+// Workspace bytes of qgemm_s8_host (qg_hostio.cu).
+size_t s8_host_workspace(int64_t M, int64_t N, int64_t K);
+
 // Host helpers (qg_api.cu).
 Ctl host_ctl(int device);  // status pointer of `device` + current timeout
 int num_sms(int device);

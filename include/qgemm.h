@@ -60,7 +60,7 @@ typedef enum { QG_ROW_MAJOR = 0, QG_COL_MAJOR = 1 } qg_layout;
 
 /* Operation ids for qg_workspace_size. */
 typedef enum {
-    QG_OP_S8 = 0, QG_OP_S4 = 1, QG_OP_F16 = 2, QG_OP_W4A16 = 3, QG_OP_W4A4 = 4
+    QG_OP_S8 = 0, QG_OP_S4 = 1, QG_OP_F16 = 2, QG_OP_W4A16 = 3, QG_OP_W4A4 = 4, QG_OP_S8_HOST = 5
 } qg_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -212,6 +212,32 @@ int qgemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
                      const int8_t *A, int64_t lda, int layout_a,
                      const int8_t *B, int64_t ldb, int layout_b,
                      int32_t *C, int64_t ldc, void *stream);
+
+/* qgemm_s8 with A, B and C in HOST memory (no counterpart on the pages; the
+ * end-to-end form of the INT8 GEMM for data that starts and ends on the host):
+ *  A : int8, M x K row-major, lda >= K      (host pointer)
+ *  B : int8, N x K row-major, ldb >= K      (host pointer)
+ *  C : int32, M x N row-major, ldc >= N     (host pointer, written)
+ *  K : multiple of 16, K < 131072.
+ *  ws: device workspace of qg_workspace_size(QG_OP_S8_HOST, M, N, K) bytes,
+ *      256-byte aligned (device copies of A, B, their fp16 forms and C).
+ * The problem is cut into pieces (up to 8 row slices of A times up to 2 row
+ * slices of B); the host-to-device copies, the conversion and GEMM of each
+ * piece, and the device-to-host copies of finished pieces run on three
+ * internal streams of the current device, so that they overlap.  Each slice
+ * crosses the link once and is converted once.  The work is ordered after
+ * what is already enqueued on `stream`, and `stream` waits for the last copy
+ * back: C is complete once `stream` has been synchronized.  Page-locked host
+ * memory keeps the copies asynchronous and at full link speed; pageable
+ * memory is accepted (the driver stages it and the call may block).  The
+ * host buffers and ws must stay valid until then.  The result is bit-exact.
+ * The internal streams are shared by all calls on a device; calls from
+ * several host threads are enqueued one at a time. */
+int qgemm_s8_host(int64_t M, int64_t N, int64_t K,
+                  const int8_t *A, int64_t lda,
+                  const int8_t *B, int64_t ldb,
+                  int32_t *C, int64_t ldc,
+                  void *ws, size_t ws_bytes, void *stream);
 
 /* [L4] Exact INT4 GEMM on s4p operands:  C = A . B^T  (int32 result).
  *  A : s4p, M x K values, lda_bytes >= K/2.

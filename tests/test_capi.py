@@ -31,6 +31,12 @@ def test_workspace_sizes(L):
     assert L.qg_workspace_size(qg.QG_OP_S4, 100, 50, 64) == 6400 + 3328
     assert L.qg_workspace_size(qg.QG_OP_F16, 512, 512, 512) == 0
     assert L.qg_workspace_size(qg.QG_OP_S8, 0, 5, 5) == 0
+    # host-memory INT8 GEMM: int8 A and B, their fp16 forms, int32 C with rows padded to 4
+    # elements, each part at a 256-byte boundary
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    M, N, K = 300, 5, 32
+    assert L.qg_workspace_size(qg.QG_OP_S8_HOST, M, N, K) == \
+        r(M * K) + r(N * K) + r(2 * M * K) + r(2 * N * K) + r(4 * M * 8)
 
 
 FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
@@ -94,3 +100,29 @@ def test_w4a16_and_w4a4_argument_errors(L):
                        WS, 16, None) == 4
     assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, None, FAKE, 4,
                        WS, big, None) == 1
+
+
+def _s8h(L, M=64, N=64, K=64, A=FAKE, lda=64, B=FAKE, ldb=64, C=FAKE, ldc=64, ws=WS, wsb=1 << 30):
+    return L.qgemm_s8_host(M, N, K, A, lda, B, ldb, C, ldc, ws, wsb, None)
+
+
+def test_qgemm_s8_host_argument_errors(L):
+    assert _s8h(L, M=0) == 1
+    assert _s8h(L, N=-1) == 1
+    assert _s8h(L, A=0) == 1
+    assert _s8h(L, C=0) == 1
+    assert _s8h(L, K=40) == 1                # K % 16
+    assert _s8h(L, K=131072, lda=131072, ldb=131072) == 1
+    assert _s8h(L, lda=32) == 1              # lda < K
+    assert _s8h(L, ldc=63) == 1              # ldc < N
+    assert _s8h(L, wsb=10) == 4              # workspace too small
+    assert _s8h(L, ws=0) == 4
+    assert _s8h(L, ws=WS + 16) == 3          # workspace not 256-byte aligned
+
+
+def test_qgemm_s8_host_without_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present (the fake host pointers would be read)")
+    # host operands need no alignment: a valid call gets as far as the device
+    assert _s8h(L, A=FAKE + 1, lda=65) == qg.QG_ERR_CUDA
