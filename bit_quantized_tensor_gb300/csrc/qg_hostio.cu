@@ -35,7 +35,7 @@ constexpr int kMaxASlices = 8;
 constexpr int kMaxBSlices = 2;
 constexpr int64_t kMinASliceRows = 1024;
 constexpr int64_t kSplitBFrom = 4096;  // N from which B is cut in two slices
-constexpr int kEvents = 2 + kMaxASlices + kMaxBSlices + kMaxASlices * kMaxBSlices;
+constexpr int kEvents = 4 + kMaxASlices + kMaxBSlices + kMaxASlices * kMaxBSlices;
 
 struct Queues {
     cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
@@ -154,8 +154,8 @@ extern "C" int qgemm_s8_host(int64_t M, int64_t N, int64_t K, const int8_t* A, i
     const Plan p = make_plan(M, N);
     const Buffers d = carve(ws, M, N, K);
     cudaStream_t user = static_cast<cudaStream_t>(stream);
-    cudaEvent_t ev_start = q->ev[0], ev_end = q->ev[1];
-    cudaEvent_t* ev_a = q->ev + 2;
+    cudaEvent_t ev_start = q->ev[0], ev_end = q->ev[1], ev_in_end = q->ev[2], ev_comp_end = q->ev[3];
+    cudaEvent_t* ev_a = q->ev + 4;
     cudaEvent_t* ev_b = ev_a + kMaxASlices;
     cudaEvent_t* ev_piece = ev_b + kMaxBSlices;
     auto rows_a = [&](int i) { return i + 1 < p.a ? p.ra : M - static_cast<int64_t>(i) * p.ra; };
@@ -213,8 +213,14 @@ extern "C" int qgemm_s8_host(int64_t M, int64_t N, int64_t K, const int8_t* A, i
         }
     }
     if (e == cudaSuccess && rc == QG_OK) {
+        // join all three queues back into the caller's stream (the copy-out
+        // queue ends last; the other two are joined explicitly so that a
+        // stream capture sees every fork closed)
         e = cudaEventRecord(ev_end, q->out);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(user, ev_end, 0);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in_end, q->in);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_comp_end, q->comp);
+        for (cudaEvent_t ev : {ev_in_end, ev_comp_end, ev_end})
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(user, ev, 0);
         if (e == cudaSuccess) return QG_OK;
     }
     // Something failed part-way: let what was enqueued finish before the

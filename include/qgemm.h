@@ -232,7 +232,10 @@ int qgemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
  * memory is accepted (the driver stages it and the call may block).  The
  * host buffers and ws must stay valid until then.  The result is bit-exact.
  * The internal streams are shared by all calls on a device; calls from
- * several host threads are enqueued one at a time. */
+ * several host threads are enqueued one at a time.  The call may be captured
+ * into a CUDA graph (its streams fork from `stream` and join back into it);
+ * while such a capture is open, make no other qgemm_s8_host call on that
+ * device, since the shared streams belong to the capture until it ends. */
 int qgemm_s8_host(int64_t M, int64_t N, int64_t K,
                   const int8_t *A, int64_t lda,
                   const int8_t *B, int64_t ldb,

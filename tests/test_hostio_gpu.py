@@ -97,3 +97,30 @@ def test_qgemm_s8_host_full_size_sampled_rows(qg, oracle):
     lhs = C.numpy().astype(np.int64) @ x
     rhs = A.astype(np.int64) @ (B.astype(np.int64).T @ x)
     assert np.array_equal(lhs, rhs)
+
+
+def test_qgemm_s8_host_in_a_cuda_graph(qg, oracle):
+    """Captured into a graph (the internal streams fork from the capturing
+    stream and join back), then replayed with new host data in place."""
+    import torch
+    M, N, K = 1200, 4300, 32
+    A = inputs.s8_uniform(M, K, 4501)
+    B = inputs.s8_uniform(N, K, 4502)
+    hA, hB = _host(A, True), _host(B, True)
+    hC = torch.empty((M, N), dtype=torch.int32).pin_memory()
+    ws = torch.empty(qg.workspace_size(qg.QG_OP_S8_HOST, M, N, K), dtype=torch.uint8, device="cuda")
+    qg.qgemm_s8_host(hA, hB, C=hC, ws=ws)  # first call on the device creates the streams
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        qg.qgemm_s8_host(hA, hB, C=hC, ws=ws, stream=s)
+    hC.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(hC.numpy(), oracle.gemm_s8(A, B))
+    A2 = inputs.s8_uniform(M, K, 4503)
+    hA.copy_(torch.from_numpy(A2))
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(hC.numpy(), oracle.gemm_s8(A2, B))
