@@ -498,6 +498,17 @@ __device__ __forceinline__ void mma_16816_c(float (&d)[4], const uint32_t (&a)[4
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
+// 16-byte shared-memory load by the lanes whose `pred` is set; the others
+// get zeros and issue no access, so a warp whose active lanes sit in one
+// quarter costs one shared-memory wavefront instead of four.
+__device__ __forceinline__ uint4 lds128_if(const void* p, bool pred) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    asm("{\n.reg .pred q;\nsetp.ne.b32 q, %5, 0;\n@q ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "r"(smem_u32(p)), "r"(static_cast<int>(pred)));
+    return v;
+}
+
 // (a ^ c) & b: the nibbles under mask b, XORed with 8 (two's complement ->
 // offset binary), nothing else: an fp16 subnormal n * 2^-24 (or 16 n * 2^-24).
 __device__ __forceinline__ uint32_t nib_sub(uint32_t a, uint32_t b, uint32_t c) {
@@ -602,8 +613,11 @@ __global__ void __launch_bounds__(kD1Threads, 2)
     const uint8_t* wrow1 = ws + r1 * L.wrs + 16 * t;
     const float* srow0 = sp + r0 * L.srs;
     const float* srow1 = sp + r1 * L.srs;
-    const uint4* xbase = g < M ? xs + g * L.xrs + t : xs + L.xrs * M;  // zero slot after the rows
-    const int xstep = g < M ? 4 : 0, xgs = g < M ? 16 : 0;
+    // Lanes of batch columns past M read nothing (zeros): with M <= 2 only
+    // the first eight lanes load X, one wavefront per load instead of four.
+    const bool xlane = g < M;
+    const uint4* xbase = xlane ? xs + g * L.xrs + t : xs + L.xrs * M;  // zero slot after the rows
+    const int xstep = xlane ? 4 : 0, xgs = xlane ? 16 : 0;
     float y[4] = {0.f, 0.f, 0.f, 0.f};
     auto group = [&](const int gi) {
         const uint4* xrow = xbase + xgs * gi;
@@ -621,7 +635,7 @@ __global__ void __launch_bounds__(kD1Threads, 2)
                                     nib_sub(ha, 0x000F000Fu, 0x00080008u), nib_sub(hb, 0x000F000Fu, 0x00080008u)};
             const uint32_t od[4] = {nib_sub(wa[i], 0x00F000F0u, 0x00800080u), nib_sub(wb[i], 0x00F000F0u, 0x00800080u),
                                     nib_sub(ha, 0x00F000F0u, 0x00800080u), nib_sub(hb, 0x00F000F0u, 0x00800080u)};
-            const uint4 xf = xrow[xstep * i];
+            const uint4 xf = lds128_if(xrow + xstep * i, xlane);
             if (i == 0) {
                 mma_16816_c(ae, ev, xf.x, xf.y, cc.x, cc.y, cc.x, cc.y);
                 mma_16816_c(ao, od, xf.z, xf.w, 0.f, 0.f, 0.f, 0.f);
