@@ -66,7 +66,7 @@ def _load():
                                               _p, _i64]),
             "orc_w4a4_gemm": (ctypes.c_int, [_i64, _i64, _i64, _p, _i64, _p, _i64,
                                              _p, _i64, _p, _i64, _i64, _p, _i64,
-                                             _p, _i64, _i64, _p, _p, _i64]),
+                                             _p, _i64, _i64, _p, _p, _p, _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -252,11 +252,12 @@ def lowrank_xu(X: np.ndarray, U: np.ndarray, nthreads: int | None = None) -> np.
 
 
 def w4a4_gemm(QX, SX, QW, SW, block: int, K: int, XU=None, V=None, bias=None,
-              nthreads: int | None = None) -> np.ndarray:
-    """Y = (Q(X).Q(W)^T) (.) scale + XU.V + b in double.
+              alpha=None, nthreads: int | None = None) -> np.ndarray:
+    """Y = alpha (.) ((Q(X).Q(W)^T) (.) scale + XU.V) + b in double.
 
     QX: M x K/2 s4p, SX: M x K/block fp16 bits, QW: N x K/2, SW: N x K/block,
-    XU: M x R double (or None), V: R x N fp16 (or None), bias: N fp16 (or None).
+    XU: M x R double (or None), V: R x N fp16 (or None), bias: N fp16 (or None),
+    alpha: N fp16 column multipliers of the affine calibration (None = 1).
     """
     QX, QW = _c(QX, np.uint8), _c(QW, np.uint8)
     SX = _c(SX.view(np.uint16) if SX.dtype == np.float16 else SX, np.uint16)
@@ -271,6 +272,9 @@ def w4a4_gemm(QX, SX, QW, SW, block: int, K: int, XU=None, V=None, bias=None,
     if bias is not None:
         bias = _c(bias.view(np.uint16) if bias.dtype == np.float16 else bias, np.uint16)
         assert bias.shape == (N,)
+    if alpha is not None:
+        alpha = _c(alpha.view(np.uint16) if alpha.dtype == np.float16 else alpha, np.uint16)
+        assert alpha.shape == (N,)
     Y = np.empty((M, N), dtype=np.float64)
     lib = _load()
 
@@ -280,6 +284,6 @@ def w4a4_gemm(QX, SX, QW, SW, block: int, K: int, XU=None, V=None, bias=None,
                                  _ptr(SW), K // block, block,
                                  _ptr(XU[r0:r1]) if R else None, R,
                                  _ptr(V) if R else None, N, R,
-                                 _ptr(bias), _ptr(Y[r0:r1]), N), "w4a4_gemm")
+                                 _ptr(alpha), _ptr(bias), _ptr(Y[r0:r1]), N), "w4a4_gemm")
     _rows_parallel(M, run, nthreads)
     return Y

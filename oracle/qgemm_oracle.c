@@ -272,7 +272,12 @@ int orc_lowrank_xu(int64_t M, int64_t K, int64_t R, const float *X, int64_t ldx,
  * sum: for block j,  sX[m][j] * sW[n][j] * sum_{k in block j} qX[m][k]*qW[n][k].
  * L(X)[m][n] = sum_r XU[m][r] * V[r][n]  (XU = X.U, given here in double).
  * b is added per output column.  XU/V (R = 0) and bias may be absent (NULL):
- * the term is then omitted. */
+ * the term is then omitted.
+ * The column-wise affine calibration ([W4A4] sections 1 and 5.2: the drain
+ * warps apply the scaling factors and a column-wise affine correction before
+ * writing) is read as the map t -> alpha[n] * t + b[n] on each output column,
+ * t being the scaled product plus L(X).  alpha (fp16, N entries) may be NULL,
+ * which means alpha = 1: the formula as printed. */
 int orc_w4a4_gemm(int64_t M, int64_t N, int64_t K,
                   const uint8_t *QX, int64_t ldqx_bytes,
                   const uint16_t *SX, int64_t ldsx,
@@ -280,7 +285,7 @@ int orc_w4a4_gemm(int64_t M, int64_t N, int64_t K,
                   const uint16_t *SW, int64_t ldsw, int64_t block,
                   const double *XU, int64_t ldxu,
                   const uint16_t *V, int64_t ldv, int64_t R,
-                  const uint16_t *bias, double *Y, int64_t ldy)
+                  const uint16_t *alpha, const uint16_t *bias, double *Y, int64_t ldy)
 {
     if (M < 0 || N < 0 || K < 0 || block <= 0 || (block & 1) || K % block ||
         ldqx_bytes < K / 2 || ldqw_bytes < K / 2 || ldsx < K / block ||
@@ -305,6 +310,8 @@ int orc_w4a4_gemm(int64_t M, int64_t N, int64_t K,
             }
             for (int64_t r = 0; r < R; ++r)
                 acc += XU[m * ldxu + r] * orc_half_to_double(V[r * ldv + n]);
+            if (alpha)
+                acc *= orc_half_to_double(alpha[n]);
             if (bias)
                 acc += orc_half_to_double(bias[n]);
             Y[m * ldy + n] = acc;

@@ -371,3 +371,57 @@ def test_w4a4_gemm_lowrank_and_bias(oracle):
     ref = (_blockwise_numpy(qx, qw, sx, sw, blk) + XU @ V.astype(np.float64)
            + b.astype(np.float64)[None, :])
     assert np.max(np.abs(Y - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+# The column-wise affine calibration of the W4A4 page (sections 1 and 5.2),
+# read as t -> alpha[n] * t + b[n] on every output column, where t is the
+# block-scaled product plus the low-rank term.
+
+def test_w4a4_gemm_unit_alpha_is_the_printed_formula(oracle):
+    M, N, K, blk, R = 4, 9, 128, 64, 32
+    qx, qw, sx, sw = _w4a4_operands(M, N, K, blk, 110)
+    XU = inputs.f32_normal(M, R, 114).astype(np.float64)
+    V = inputs.f16_normal(R, N, 115, sigma=0.02)
+    b = inputs.f16_normal(1, N, 116, sigma=0.1)[0]
+    args = (oracle.s4_pack(qx), sx, oracle.s4_pack(qw), sw, blk, K)
+    Y0 = oracle.w4a4_gemm(*args, XU=XU, V=V, bias=b)
+    Y1 = oracle.w4a4_gemm(*args, XU=XU, V=V, bias=b, alpha=np.ones(N, dtype=np.float16))
+    assert np.array_equal(Y0, Y1)
+
+
+def test_w4a4_gemm_alpha_scales_product_and_lowrank_not_bias(oracle):
+    M, N, K, blk, R = 5, 12, 192, 64, 32
+    qx, qw, sx, sw = _w4a4_operands(M, N, K, blk, 120, pow2_scales=True)
+    # alpha and every other operand exact in binary: the result is exact
+    alpha = (2.0 ** inputs.s8_in_range(1, N, -3, 3, 121)[0].astype(np.float64)).astype(np.float16)
+    XU = inputs.s8_in_range(M, R, -4, 4, 124).astype(np.float64)
+    V = (inputs.s8_in_range(R, N, -4, 4, 125).astype(np.float64) / 8).astype(np.float16)
+    b = (inputs.s8_in_range(1, N, -16, 16, 126)[0].astype(np.float64) / 4).astype(np.float16)
+    Y = oracle.w4a4_gemm(oracle.s4_pack(qx), sx, oracle.s4_pack(qw), sw, blk, K,
+                         XU=XU, V=V, bias=b, alpha=alpha)
+    a = alpha.astype(np.float64)[None, :]
+    t = _blockwise_numpy(qx, qw, sx, sw, blk) + XU @ V.astype(np.float64)
+    assert np.array_equal(Y, a * t + b.astype(np.float64)[None, :])
+    # zero codes: only the low-rank term, scaled by alpha, plus the bias
+    z = np.zeros_like(qx)
+    Yz = oracle.w4a4_gemm(oracle.s4_pack(z), sx, oracle.s4_pack(qw), sw, blk, K,
+                          XU=XU, V=V, bias=b, alpha=alpha)
+    assert np.array_equal(Yz, a * (XU @ V.astype(np.float64)) + b.astype(np.float64)[None, :])
+    # no low-rank term, no bias: alpha times the block-scaled product
+    Yp = oracle.w4a4_gemm(oracle.s4_pack(qx), sx, oracle.s4_pack(qw), sw, blk, K, alpha=alpha)
+    assert np.array_equal(Yp, a * _blockwise_numpy(qx, qw, sx, sw, blk))
+
+
+def test_w4a4_gemm_alpha_matches_numpy(oracle):
+    M, N, K, blk, R = 6, 10, 256, 64, 32
+    qx, qw, sx, sw = _w4a4_operands(M, N, K, blk, 130)
+    alpha = inputs.f16_uniform(1, N, 0.5, 2.0, 131)[0]
+    XU = inputs.f32_normal(M, R, 134).astype(np.float64)
+    V = inputs.f16_normal(R, N, 135, sigma=0.02)
+    b = inputs.f16_normal(1, N, 136, sigma=0.1)[0]
+    Y = oracle.w4a4_gemm(oracle.s4_pack(qx), sx, oracle.s4_pack(qw), sw, blk, K,
+                         XU=XU, V=V, bias=b, alpha=alpha)
+    ref = (alpha.astype(np.float64)[None, :]
+           * (_blockwise_numpy(qx, qw, sx, sw, blk) + XU @ V.astype(np.float64))
+           + b.astype(np.float64)[None, :])
+    assert np.max(np.abs(Y - ref)) <= 1e-12 * np.max(np.abs(ref))
