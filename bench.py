@@ -68,6 +68,7 @@ ABLATIONS = {
     "gemm_path": ("qg_set_gemm_path", (0, 1, 2), ("s8", "s4", "f16", "w4a4_gemm")),
     "pdl": ("qg_set_pdl", (1, 0), ("w4a16", "w4a16_m16", "w4a16_m128")),
     "s8_chunk": ("qg_set_s8_chunk", (16, 8, 4), ("s8",)),
+    "l2_policy": ("qg_set_l2_policy", (0, 1, 2), ("s8", "s4", "f16")),
 }
 
 

@@ -12,6 +12,8 @@ Functions (same names as the C ABI):
   w4a16_gemm(X, Wq, Wscale) weight-only INT4 linear, per-group (128) fp16 scales
   w4a4_quantize(X, U)       per-row, per-64-block absmax INT4 quantizer (+ X.U)
   w4a4_gemm(...)            Y = (Q(X).Q(W)^T) (.) scale + (X.U).V + b
+                            (alpha=...: the column-wise affine form,
+                            Y = alpha (.) (...) + b, through w4a4_gemm_affine)
 B / W operands are K-major (N x K row-major), the layout every call takes.
 """
 from __future__ import annotations
@@ -68,6 +70,7 @@ SIGNATURES = {
     "qg_kernel_budget_measure": (_int, [_int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_gemm_path": (_int, [_int]),
+    "qg_set_l2_policy": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
     "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
@@ -79,6 +82,8 @@ SIGNATURES = {
     "w4a4_quantize": (_int, [_i64, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _p]),
     "w4a4_gemm": (_int, [_i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _i64, _p, _p, _i64,
                          _p, _sz, _p]),
+    "w4a4_gemm_affine": (_int, [_i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _i64, _p, _p, _p,
+                                _i64, _p, _sz, _p]),
 }
 
 _lib = None
@@ -331,11 +336,12 @@ def w4a4_quantize(X, Ut=None, block: int = 64, out=None, stream=None):
 
 
 def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, Vt=None, bias=None, block: int = 64,
-              Y=None, ws=None, stream=None):
+              Y=None, ws=None, stream=None, alpha=None):
     """Y = (Q(X).Q(W)^T) (.) scale + XU . Vt^T + bias, fp16 M x N.
 
     Vt is the low-rank up-projection transposed (N x rank fp16, the weight of
-    a rank -> N linear layer).
+    a rank -> N linear layer).  With alpha (N fp16 column multipliers) the
+    call is w4a4_gemm_affine: Y = alpha (.) ((...) (.) scale + XU . Vt^T) + bias.
     """
     torch = _torch()
     V = Vt
@@ -353,13 +359,20 @@ def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, Vt=None, bias=None, block
             raise ValueError("Vt must be a contiguous N x rank fp16 matrix")
     if bias is not None:
         _cuda(bias, torch.float16, "bias")
+    if alpha is not None:
+        _cuda(alpha, torch.float16, "alpha")
+        if alpha.numel() != N:
+            raise ValueError("alpha must hold N fp16 column multipliers")
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float16, device=Xq.device)
     _cuda(Y, torch.float16, "Y")
     ws, wsb = _workspace(QG_OP_W4A4, M, N, K, Xq.device, ws)
-    _check("w4a4_gemm", lib().w4a4_gemm(
-        M, N, K, Xq.data_ptr(), Xscale.data_ptr(), Wq.data_ptr(), Wscale.data_ptr(), block,
-        XU.data_ptr() if rank else None, V.data_ptr() if rank else None, rank,
-        bias.data_ptr() if bias is not None else None, Y.data_ptr(), Y.stride(0),
-        ws.data_ptr(), wsb, _stream(stream)))
+    head = (M, N, K, Xq.data_ptr(), Xscale.data_ptr(), Wq.data_ptr(), Wscale.data_ptr(), block,
+            XU.data_ptr() if rank else None, V.data_ptr() if rank else None, rank)
+    tail = (bias.data_ptr() if bias is not None else None, Y.data_ptr(), Y.stride(0),
+            ws.data_ptr(), wsb, _stream(stream))
+    if alpha is None:
+        _check("w4a4_gemm", lib().w4a4_gemm(*head, *tail))
+    else:
+        _check("w4a4_gemm_affine", lib().w4a4_gemm_affine(*head, alpha.data_ptr(), *tail))
     return Y

@@ -76,6 +76,11 @@ void profile_events(void** before, void** after) {
     *after = g_prof_after.load();
 }
 
+// L2 policy mode of the tensor-core GEMM kernels (qg_set_l2_policy): 0 =
+// evict-normal loads, 1 = A evict-last / B evict-first, 2 = as 1 plus
+// streaming output stores.
+static std::atomic<int> g_l2_mode{0};
+
 template <class Cfg>
 static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ldb_bytes, int64_t M,
                      int64_t N, int64_t K, void* C, int64_t ldc, int chunk_kb, const __half* bias,
@@ -112,6 +117,7 @@ static int launch_tc(const void* A, int64_t lda_bytes, const void* B, int64_t ld
     p.ldc = ldc;
     p.bias = bias;
     p.ctl = ctl;
+    p.l2_mode = g_l2_mode.load();
     const int64_t tiles = ((M + Cfg::BM - 1) / Cfg::BM) * ((N + Cfg::BN - 1) / Cfg::BN);
     const int grid = static_cast<int>(tiles < num_sms(dev) ? tiles : num_sms(dev));
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_prof_before.load());
@@ -158,6 +164,7 @@ static int launch_tc2(const void* A, int64_t lda_bytes, const void* B, int64_t l
     p.ldc = ldc;
     p.bias = bias;
     p.ctl = ctl;
+    p.l2_mode = g_l2_mode.load();
     const int64_t tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
     const int64_t max_pairs = num_sms(dev) / 2;
     const int grid = 2 * static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
@@ -426,6 +433,12 @@ int qg_set_profile_events(void* before, void* after) {
 int qg_set_gemm_path(int path) {
     if (path < 0 || path > 2) return QG_ERR_INVALID_ARG;
     g_gemm_path.store(path);
+    return QG_OK;
+}
+
+int qg_set_l2_policy(int mode) {
+    if (mode < 0 || mode > 2) return QG_ERR_INVALID_ARG;
+    g_l2_mode.store(mode);
     return QG_OK;
 }
 

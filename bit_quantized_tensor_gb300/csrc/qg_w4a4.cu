@@ -326,15 +326,25 @@ __global__ void __launch_bounds__(kQThreads, 2)
 
 // St[j][r] = S[r][j] (fp16 -> fp32) for j < nblk; St[nblk][r] = 1; columns
 // r in [rows, rows_p) are 0.  S: rows x nblk, St: (nblk + 1) x rows_p.
+// With `alpha` (one fp16 multiplier per row of S, i.e. per output column of
+// the GEMM) every entry of row r, the constant one included, is multiplied by
+// alpha[r]: that applies the column-wise affine calibration's multiplier to
+// both the block-scaled product and the low-rank unit.  An fp16 scale times
+// an fp16 multiplier has at most 22 significant bits, so the fp32 product is
+// exact.
 __global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
-                                    const __half* __restrict__ S, float* __restrict__ St) {
+                                    const __half* __restrict__ S, const __half* __restrict__ alpha,
+                                    float* __restrict__ St) {
     const int64_t total = static_cast<int64_t>(nblk + 1) * rows_p;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t j = i / rows_p;
         const int64_t r = i - j * rows_p;
         float v = 0.f;
-        if (r < rows) v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
+        if (r < rows) {
+            v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
+            if (alpha) v *= __half2float(alpha[r]);
+        }
         St[i] = v;
     }
 }
@@ -467,11 +477,15 @@ int w4a4_quantize(int64_t M, int64_t K, const float* X, int64_t ldx, const uint1
     return map_cuda(cudaGetLastError());
 }
 
-int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
-              const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
-              const uint16_t* V, int64_t rank, const uint16_t* bias, uint16_t* Y, int64_t ldy,
-              void* ws, size_t ws_bytes, void* stream) {
-    const qg::NvtxRange nvtx_range("w4a4_gemm");
+}  // extern "C"
+
+namespace qg {
+
+// w4a4_gemm and w4a4_gemm_affine: alpha == nullptr is the formula as printed.
+static int w4a4_gemm_impl(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
+                          const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
+                          const uint16_t* V, int64_t rank, const uint16_t* alpha, const uint16_t* bias,
+                          uint16_t* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
     if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return QG_ERR_INVALID_ARG;
     if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;
@@ -503,9 +517,10 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     int rc = s4_to_e4m3_pair(Xq, M, K / 2, A8, Wq, N, K / 2, B8, K, dev, s);
     if (rc) return rc;
     k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
-        M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), SXt);
+        M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), nullptr, SXt);
     k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
-        N, Np, nblk, reinterpret_cast<const __half*>(Wscale), SWt);
+        N, Np, nblk, reinterpret_cast<const __half*>(Wscale), reinterpret_cast<const __half*>(alpha),
+        SWt);
     rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
 
@@ -524,6 +539,29 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t
     const bool pairs = path == 2 || (path == 0 && M > W4A4Cfg::BM);
     return pairs ? launch_w4a4<W4A4PairCfg, true>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s)
                  : launch_w4a4<W4A4Cfg, false>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s);
+}
+
+}  // namespace qg
+
+extern "C" {
+
+int w4a4_gemm(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
+              const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
+              const uint16_t* V, int64_t rank, const uint16_t* bias, uint16_t* Y, int64_t ldy,
+              void* ws, size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_gemm");
+    return w4a4_gemm_impl(M, N, K, Xq, Xscale, Wq, Wscale, block, XU, V, rank, nullptr, bias, Y, ldy,
+                          ws, ws_bytes, stream);
+}
+
+int w4a4_gemm_affine(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
+                     const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
+                     const uint16_t* V, int64_t rank, const uint16_t* alpha, const uint16_t* bias,
+                     uint16_t* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_gemm_affine");
+    if (!alpha) return QG_ERR_INVALID_ARG;
+    return w4a4_gemm_impl(M, N, K, Xq, Xscale, Wq, Wscale, block, XU, V, rank, alpha, bias, Y, ldy,
+                          ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -93,7 +93,34 @@ struct TcGemmParams {
     int64_t ldc;    // in elements
     const __half* bias;  // optional per-column bias (F16 epilogue), may be null
     Ctl ctl;
+    int l2_mode;    // L2 policy of the operand loads and output stores (qg_set_l2_policy)
 };
+
+// L2 policies of one GEMM launch.  Mode 0: every TMA load evict-normal.
+// Modes 1 and 2 follow the tile order below: a group of row-blocks is
+// finished against every column block before the next group starts, so an
+// A tile is read again in later rounds (evict-last) while a B tile is read by
+// the row-blocks of one group at about the same time and then not for a
+// whole group (evict-first).  Mode 2 also writes the output with streaming
+// (evict-first) stores, which are not read again by this kernel.
+struct L2Policies {
+    uint64_t a, b;
+};
+__device__ __forceinline__ L2Policies l2_policies(int mode) {
+    if (mode == 0) {
+        const uint64_t n = l2_policy_evict_normal();
+        return {n, n};
+    }
+    return {l2_policy_evict_last(), l2_policy_evict_first()};
+}
+
+// 16-byte global store, with the streaming (evict-first) hint when `cs`.
+__device__ __forceinline__ void st_global_16(void* dst, uint4 v, bool cs) {
+    if (cs)
+        __stcs(reinterpret_cast<uint4*>(dst), v);
+    else
+        *reinterpret_cast<uint4*>(dst) = v;
+}
 
 // Tiles are visited in groups of `group_m` row-blocks (column-major inside a
 // group) so that the CTAs running at the same time cover a compact block of
@@ -114,7 +141,7 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
 
 template <int N>
 __device__ __forceinline__ void store_row_f16(__half* dst, int col0, int N_total, const float* v,
-                                              const __half* bias) {
+                                              const __half* bias, bool cs = false) {
 #pragma unroll
     for (int c = 0; c < N; c += 8) {
         float f[8];
@@ -137,7 +164,7 @@ __device__ __forceinline__ void store_row_f16(__half* dst, int col0, int N_total
             pk.y = *reinterpret_cast<uint32_t*>(&h1);
             pk.z = *reinterpret_cast<uint32_t*>(&h2);
             pk.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(dst + c) = pk;
+            st_global_16(dst + c, pk, cs);
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -148,11 +175,14 @@ __device__ __forceinline__ void store_row_f16(__half* dst, int col0, int N_total
 
 template <int N>
 __device__ __forceinline__ void store_row_s32(int32_t* dst, int col0, int N_total,
-                                              const int32_t* v) {
+                                              const int32_t* v, bool cs = false) {
 #pragma unroll
     for (int c = 0; c < N; c += 4) {
         if (col0 + c + 4 <= N_total && (reinterpret_cast<uintptr_t>(dst + c) & 15u) == 0) {
-            *reinterpret_cast<int4*>(dst + c) = make_int4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+            st_global_16(dst + c,
+                         make_uint4(static_cast<uint32_t>(v[c]), static_cast<uint32_t>(v[c + 1]),
+                                    static_cast<uint32_t>(v[c + 2]), static_cast<uint32_t>(v[c + 3])),
+                         cs);
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -216,7 +246,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // ------------------------------------------------ TMA producer
             PipeState<STAGES> ps;
             uint32_t armed = 0, armed_phase = 0;  // bit s: slot s armed / its phase
-            const uint64_t pol = l2_policy_evict_normal();
+            const L2Policies pol = l2_policies(p.l2_mode);
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
                 int mb, nb;
@@ -229,9 +259,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(ps.index), Cfg::STAGE_BYTES);
                     tma_load_2d(smem_u32(sA + ps.index * Cfg::A_BYTES), &tmA, kb * Cfg::BK,
-                                mb * Cfg::BM, full_bar(ps.index), pol);
+                                mb * Cfg::BM, full_bar(ps.index), pol.a);
                     tma_load_2d(smem_u32(sB + ps.index * Cfg::B_BYTES), &tmB, kb * Cfg::BK,
-                                nb * Cfg::BN, full_bar(ps.index), pol);
+                                nb * Cfg::BN, full_bar(ps.index), pol.b);
                     armed |= 1u << ps.index;
                     armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
                     ps.advance();
@@ -334,7 +364,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (row < p.M)
                     store_row_s32<128>(static_cast<int32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,
-                                       col0, p.N, sum);
+                                       col0, p.N, sum, p.l2_mode == 2);
             } else {
                 bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
                                         kSiteEpiAccFull);
@@ -361,7 +391,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (row < p.M)
                     store_row_f16<128>(static_cast<__half*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,
-                                       col0, p.N, v, p.bias);
+                                       col0, p.N, v, p.bias, p.l2_mode == 2);
             }
         }
     }

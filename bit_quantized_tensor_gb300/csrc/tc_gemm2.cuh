@@ -129,7 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             // ------------------------------------------------ TMA producer (both CTAs)
             PipeState<STAGES> ps;
             uint32_t armed = 0, armed_phase = 0;
-            const uint64_t pol = l2_policy_evict_normal();
+            const L2Policies pol = l2_policies(p.l2_mode);
             bool ok = true;
             for (int t = pair; ok && t < ntiles; t += npairs) {
                 int mb, nb;
@@ -149,9 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                         armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
                     }
                     tma_load_2d_pair(smem_u32(sA + ps.index * Cfg::A_BYTES), &tmA, kb * Cfg::BK, arow,
-                                     lead_full, pol);
+                                     lead_full, pol.a);
                     tma_load_2d_pair(smem_u32(sB + ps.index * Cfg::B_BYTES), &tmB, kb * Cfg::BK, brow,
-                                     lead_full, pol);
+                                     lead_full, pol.b);
                     ps.advance();
                 }
             }
@@ -258,7 +258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 if (row < p.M)
                     store_row_s32<128>(static_cast<int32_t*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,
-                                       col0, p.N, sum);
+                                       col0, p.N, sum, p.l2_mode == 2);
             } else {
                 bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
                                         kSitePairEpiAcc);
@@ -285,7 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 if (row < p.M)
                     store_row_f16<128>(static_cast<__half*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,
-                                       col0, p.N, v, p.bias);
+                                       col0, p.N, v, p.bias, p.l2_mode == 2);
             }
         }
     }

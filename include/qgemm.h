@@ -160,6 +160,18 @@ int qg_set_s8_chunk(int kblocks);
  * 2 = always CTA pairs.  Results are identical; only speed differs. */
 int qg_set_gemm_path(int path);
 
+/* L2 cache policy of the tensor-core GEMMs behind gemm_f16, qgemm_s8 and
+ * qgemm_s4 (an ablation knob; results are identical in every mode):
+ *   0 = every TMA operand load evict-normal (default);
+ *   1 = A tiles evict-last, B tiles evict-first: the kernels finish a group
+ *       of row-blocks against every column block before the next group, so
+ *       an A tile is read again in later rounds while a B tile is read by the
+ *       group's row-blocks at about the same time and then not for a whole
+ *       group;
+ *   2 = as 1, and the output written with streaming (evict-first) stores.
+ * QG_ERR_INVALID_ARG for another mode. */
+int qg_set_l2_policy(int mode);
+
 /* Programmatic dependent launch of w4a16_gemm (default on).  When on, a
  * w4a16_gemm kernel may start while the previous kernel on the stream is
  * still running: it streams Wq and Wscale at once and reads X only after
@@ -320,6 +332,25 @@ int w4a4_gemm(int64_t M, int64_t N, int64_t K,
               const uint16_t *XU, const uint16_t *V, int64_t rank,
               const uint16_t *bias, uint16_t *Y, int64_t ldy,
               void *ws, size_t ws_bytes, void *stream);
+
+/* [W4A4] w4a4_gemm with the column-wise affine calibration that the page's
+ * drain warps apply before writing (sections 1 and 5.2), read as the map
+ * t -> alpha[n] * t + bias[n] on every output column:
+ *  Y[m][n] = alpha[n] * ( sum_j Xscale[m][j]*Wscale[n][j] * sum_{k in block j} Xq[m][k]*Wq[n][k]
+ *                        + sum_r XU[m][r] * V[r][n] ) + bias[n].
+ *  alpha : fp16, N column multipliers, device memory, not NULL (w4a4_gemm is
+ *          the case alpha = 1).  Every other argument, layout, workspace and
+ *          error as in w4a4_gemm.
+ * The multiplier is folded into the fp32 copy of Wscale that the call builds
+ * in its workspace (an fp16 scale times an fp16 multiplier is exact in fp32),
+ * so it costs no extra pass and no extra work in the GEMM kernel. */
+int w4a4_gemm_affine(int64_t M, int64_t N, int64_t K,
+                     const uint8_t *Xq, const uint16_t *Xscale,
+                     const uint8_t *Wq, const uint16_t *Wscale, int64_t block,
+                     const uint16_t *XU, const uint16_t *V, int64_t rank,
+                     const uint16_t *alpha, const uint16_t *bias,
+                     uint16_t *Y, int64_t ldy,
+                     void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

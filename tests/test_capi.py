@@ -100,6 +100,13 @@ def test_w4a16_and_w4a4_argument_errors(L):
                        WS, 16, None) == 4
     assert L.w4a4_gemm(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, None, FAKE, 4,
                        WS, big, None) == 1
+    # w4a4_gemm_affine(M, N, K, Xq, Xs, Wq, Ws, block, XU, V, rank, alpha, bias, Y, ldy, ws, wsb, stream)
+    assert L.w4a4_gemm_affine(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, None, None,
+                              FAKE, 8, WS, big, None) == 1  # alpha is required
+    assert L.w4a4_gemm_affine(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 32, None, None, 0, FAKE, None,
+                              FAKE, 8, WS, big, None) == 2
+    assert L.w4a4_gemm_affine(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, FAKE, None,
+                              FAKE, 8, WS, 16, None) == 4
 
 
 def _s8h(L, M=64, N=64, K=64, A=FAKE, lda=64, B=FAKE, ldb=64, C=FAKE, ldc=64, ws=WS, wsb=1 << 30):
@@ -126,3 +133,12 @@ def test_qgemm_s8_host_without_gpu_reports_cuda_error(L):
         pytest.skip("a GPU is present (the fake host pointers would be read)")
     # host operands need no alignment: a valid call gets as far as the device
     assert _s8h(L, A=FAKE + 1, lda=65) == qg.QG_ERR_CUDA
+
+
+def test_knob_ranges(L):
+    # host-side setters: out-of-range values are refused, defaults restored
+    assert L.qg_set_l2_policy(3) == 1 and L.qg_set_l2_policy(-1) == 1
+    for m in (1, 2, 0):
+        assert L.qg_set_l2_policy(m) == 0
+    assert L.qg_set_gemm_path(3) == 1 and L.qg_set_gemm_path(0) == 0
+    assert L.qg_set_s8_chunk(0) == 1 and L.qg_set_s8_chunk(17) == 1 and L.qg_set_s8_chunk(16) == 0

@@ -253,3 +253,41 @@ def test_paths_gemm_f16(dev, oracle, gemm_path, path, M, N, K):
     B = inputs.f16_normal(N, K, 2700 + N)
     C = qg.gemm_f16(_t(A, dev), _t(B, dev)).cpu().numpy()
     assert_fp16_close(C, oracle.gemm_f16(A, B), f"gemm_f16 path {path} {M}x{N}x{K}")
+
+
+# ------------------------------------------------- L2 cache-policy modes
+
+@pytest.fixture
+def l2_policy():
+    import bit_quantized_tensor_gb300 as qg
+    def set_mode(m):
+        assert qg.lib().qg_set_l2_policy(m) == 0
+    yield set_mode
+    qg.lib().qg_set_l2_policy(0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("path", [1, 2])
+def test_l2_policy_modes_same_results(dev, oracle, gemm_path, l2_policy, mode, path):
+    """The cache hints change only where lines live in L2: the integer GEMMs
+    stay bit-exact and the fp16 GEMM gives the same bits as mode 0."""
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    M, N, K = 520, 1000, 1056
+    A = inputs.s8_uniform(M, K, 1800)
+    B = inputs.s8_uniform(N, K, 2800)
+    A4 = inputs.s4_packed_uniform(M, K, 1801)
+    B4 = inputs.s4_packed_uniform(N, K, 2801)
+    Af = inputs.f16_normal(M, K, 1802)
+    Bf = inputs.f16_normal(N, K, 2802)
+    l2_policy(0)
+    f0 = qg.gemm_f16(_t(Af, dev), _t(Bf, dev)).cpu().numpy()
+    l2_policy(mode)
+    C8 = _s8(dev, A, B)
+    ref = oracle.gemm_s8(A, B)
+    assert np.array_equal(C8, ref), first_mismatch(C8, ref)
+    C4 = _s4(dev, A4, B4, K)
+    ref4 = oracle.gemm_s4(A4, B4, K)
+    assert np.array_equal(C4, ref4), first_mismatch(C4, ref4)
+    f1 = qg.gemm_f16(_t(Af, dev), _t(Bf, dev)).cpu().numpy()
+    assert np.array_equal(f0.view(np.uint16), f1.view(np.uint16))

@@ -194,6 +194,46 @@ def test_gemm_unit_scales_equal_int4_gemm(dev, oracle, gemm_path, path):
     assert np.array_equal(Y.astype(np.float64), oracle.gemm_s4(qx, qw, K).astype(np.float64))
 
 
+AFFINE_SHAPES = [(1, 8, 64, 32, True), (100, 300, 256, 32, True), (300, 136, 192, 0, False),
+                 (520, 392, 1088, 32, True)]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K,rank,bias", AFFINE_SHAPES)
+def test_gemm_affine_matches_oracle(dev, oracle, gemm_path, path, M, N, K, rank, bias):
+    """Column-wise affine calibration: Y = alpha (.) (scaled product + L(X)) + b."""
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    X, W, U, V, b = _gemm_case(M, N, K, 11, rank, bias)
+    alpha = inputs.f16_uniform(1, N, 0.25, 4.0, 3300 + M)[0]
+    qx, sx = oracle.w4a4_quantize(X, BLOCK)
+    qw, sw = oracle.w4a4_quantize(W, BLOCK)
+    xu16 = oracle.lowrank_xu(X, U).astype(np.float16) if rank else None
+    Y = qg.w4a4_gemm(_t(qx, dev), _t(sx.view(np.float16), dev), _t(qw, dev),
+                     _t(sw.view(np.float16), dev), K,
+                     XU=_t(xu16, dev) if rank else None, Vt=_t(V.T, dev) if rank else None,
+                     bias=_t(b, dev) if bias else None, alpha=_t(alpha, dev)).cpu().numpy()
+    ref = oracle.w4a4_gemm(qx, sx, qw, sw, BLOCK, K,
+                           XU=xu16.astype(np.float64) if rank else None,
+                           V=V if rank else None, bias=b if bias else None, alpha=alpha)
+    assert_fp16_close(Y, ref, f"w4a4 affine {M}x{N}x{K} r={rank}")
+
+
+def test_gemm_affine_unit_alpha_equals_plain_call(dev, oracle):
+    """alpha = 1 gives bit for bit the plain w4a4_gemm result."""
+    import bit_quantized_tensor_gb300 as qg
+    M, N, K = 260, 384, 512
+    X, W, U, V, b = _gemm_case(M, N, K, 12)
+    tX, tW = _t(X, dev), _t(W, dev)
+    qx, sx, xu = qg.w4a4_quantize(tX, _t(U.T, dev), BLOCK)
+    qw, sw, _ = qg.w4a4_quantize(tW, None, BLOCK)
+    Vt, tb = _t(V.T, dev), _t(b, dev)
+    Y0 = qg.w4a4_gemm(qx, sx, qw, sw, K, XU=xu, Vt=Vt, bias=tb).cpu().numpy()
+    one = _t(np.ones(N, dtype=np.float16), dev)
+    Y1 = qg.w4a4_gemm(qx, sx, qw, sw, K, XU=xu, Vt=Vt, bias=tb, alpha=one).cpu().numpy()
+    assert np.array_equal(Y0.view(np.uint16), Y1.view(np.uint16))
+
+
 def test_end_to_end_full_size_sampled(dev, oracle):
     """The W4A4 workload (M=4096, N=K=8192, rank 32): GPU quantizer + GPU GEMM
     against the oracle's quantize -> X.U -> block-scaled GEMM on sampled rows."""
