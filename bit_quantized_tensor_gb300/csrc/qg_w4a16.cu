@@ -52,6 +52,20 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
     return v;
 }
 
+// 16 bytes of X.  X may be the output of the kernel launched just before
+// (programmatic dependent launch), so it must be read only after
+// griddepcontrol.wait.  A __ldg is an invariant load that the compiler may
+// hoist above that wait; this load is a volatile asm statement, which keeps
+// its place after the wait (also a volatile asm statement).  It is a plain
+// weak load: after the wait the prior grid's writes are visible to this grid.
+__device__ __forceinline__ uint4 ld_x_u4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ unsigned short ld_nc_u16(const void* p) {
     unsigned short v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -83,7 +97,7 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&p)[4]) {
 // X fragment words for physical k = k0 .. k0+7 of one row, regrouped as the
 // pairs (x0,x4), (x1,x5), (x2,x6), (x3,x7).
 __device__ __forceinline__ void x_pairs(const __half* row, uint32_t (&p)[4]) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row));
+    const uint4 v = ld_x_u4(row);
     p[0] = __byte_perm(v.x, v.z, 0x5410);
     p[1] = __byte_perm(v.x, v.z, 0x7632);
     p[2] = __byte_perm(v.y, v.w, 0x5410);
@@ -352,8 +366,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
             const int m = mb * 8 + g;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                xf[mb][i] = m < M ? x_pairs(__ldg(reinterpret_cast<const uint4*>(
-                                        X + static_cast<int64_t>(m) * ldx + gi * kGroup + 32 * t + 8 * i)))
+                xf[mb][i] = m < M ? x_pairs(ld_x_u4(
+                                        X + static_cast<int64_t>(m) * ldx + gi * kGroup + 32 * t + 8 * i))
                                   : make_uint4(0u, 0u, 0u, 0u);
         }
         uint4 w0 = make_uint4(0u, 0u, 0u, 0u);  // nibbles 0: rows past N contribute 0
@@ -574,7 +588,7 @@ __global__ void __launch_bounds__(kD1Threads, 2)
             const int c8 = cb + lane;
             const bool ok = c8 < K8;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (ok) v = __ldg(reinterpret_cast<const uint4*>(xr + 8 * c8));
+            if (ok) v = ld_x_u4(xr + 8 * c8);
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
             float sum = 0.f;
 #pragma unroll
@@ -778,9 +792,9 @@ __global__ void __launch_bounds__(kD2Threads, 2)
     auto load_x = [&](int gi, uint4 (&xf)[2][4]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            xf[0][i] = xv0 ? x_pairs(__ldg(reinterpret_cast<const uint4*>(xr0 + gi * kGroup + 8 * i)))
+            xf[0][i] = xv0 ? x_pairs(ld_x_u4(xr0 + gi * kGroup + 8 * i))
                            : make_uint4(0u, 0u, 0u, 0u);
-            xf[1][i] = xv1 ? x_pairs(__ldg(reinterpret_cast<const uint4*>(xr1 + gi * kGroup + 8 * i)))
+            xf[1][i] = xv1 ? x_pairs(ld_x_u4(xr1 + gi * kGroup + 8 * i))
                            : make_uint4(0u, 0u, 0u, 0u);
         }
     };
