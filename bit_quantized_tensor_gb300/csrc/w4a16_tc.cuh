@@ -7,25 +7,25 @@
 // batch rows and splits K four ways: CTA r handles a contiguous quarter of
 // the K groups.  Per 64-wide K stage a CTA
 //  - TMA-loads its 128 x 64 fp16 tile of X and its 128 rows x 32 bytes of
-//    packed weights into a 5-deep ring (every cluster re-reads X from L2,
+//    packed weights into an 8-deep ring (every cluster re-reads X from L2,
 //    and a load took about 2000 cycles to land under that traffic);
-//  - turns the nibbles into two exact fp16 operand
-//    rows per weight row, q * s_hi and q * s_lo, where s_hi is the group scale
-//    with its three lowest mantissa bits cleared and s_lo = s - s_hi: q has at
-//    most three significant bits, so both products are exact in fp16 and
-//    q * s_hi + q * s_lo = q * s (rounding q * s to fp16, a plain
-//    dequantize-then-GEMM, costs up to 2^-12 of every weight); the 256 rows go
-//    to the 128-byte-swizzled K-major layout of the MMA's B operand, in a
-//    ring of three slots (with two, the transform of a stage waited for the
-//    MMA two stages back to complete, which paced the loop).  Two groups of
-//    eight warps take alternate stages: one warp's pass over a stage is
-//    latency-bound (shared-memory loads, the proxy fence, the barrier
-//    arrival), so two stages in flight double the transform rate;
-//  - issues tcgen05.mma kind::f16 M=128 N=256 (one thread) into a 256-column
-//    TMEM accumulator.  Every product is exact in fp32, so the only rounding
-//    is the fp32 accumulation.  Wide MMAs matter here: an instruction costs
-//    about 128 cycles whatever its width, so N=64 ran at a quarter of the rate.
-// At the end every CTA adds its hi and lo halves into a 128 x 128 fp32
+//  - dequantizes in registers, as the SM75 page does: each weight becomes
+//    the fp16 product q * s (rounded once, at most 2^-11 of the weight); the
+//    128 rows go to the 128-byte-swizzled K-major layout of the MMA's B
+//    operand, in a ring of three slots (with two, the transform of a stage
+//    waited for the MMA two stages back to complete, which paced the loop).
+//    Two groups of eight warps take alternate stages: one warp's pass over a
+//    stage is latency-bound (shared-memory loads, the proxy fence, the
+//    barrier arrival), so two stages in flight double the transform rate;
+//  - issues tcgen05.mma kind::f16 M=128 N=128 (one thread) into a 128-column
+//    TMEM accumulator.
+// The loop is bound by shared-memory traffic: per stage the ring takes X and
+// the packed rows, the transform writes the B operand and the MMA reads X and
+// B.  An exact alternative (q * s split into two exact fp16 rows, q * s_hi
+// and q * s_lo, with s_hi the scale with its three lowest mantissa bits
+// cleared) doubles the B operand, 104 KB of shared-memory traffic per stage
+// against 72 KB here, and was slower by that much.
+// At the end every CTA stores its 128 x 128 fp32
 // partial tile in shared memory and, once every CTA of the cluster is past
 // its K loop, bulk-copies rows [32 r, 32 r + 32) of it into CTA r's shared
 // memory (the copy engine signals CTA r's barrier with the byte count); CTA r
@@ -34,7 +34,7 @@
 // with release semantics cost about half a microsecond here, as much as the
 // whole exchange.  Weight rows and scales are fetched before the
 // programmatic dependent wait; X after it.  Every wait is bounded.  Scales
-// must stay below 8192 in magnitude (8 * s_hi must be a finite fp16).
+// must stay below 8188 in magnitude (8 * s must be a finite fp16).
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -72,16 +72,16 @@ struct W16TcCfg {
     static constexpr int BN = 128;                      // weight rows (output columns) per cluster
     static constexpr int BK = 64;                       // K per stage: 128 bytes of fp16
     static constexpr int X_BYTES = BM * BK * 2;         // 16 KB
-    static constexpr int B_ROWS = 2 * BN;               // q * s_hi rows, then q * s_lo rows
-    static constexpr int B_BYTES = B_ROWS * BK * 2;     // 32 KB fp16 operand
+    static constexpr int B_ROWS = BN;                   // q * s rows
+    static constexpr int B_BYTES = B_ROWS * BK * 2;     // 16 KB fp16 operand
     static constexpr int W_BYTES = BN * BK / 2;         // 4 KB packed nibbles
-    static constexpr int STAGES = 5;                    // X + packed-weight ring (memory latency)
+    static constexpr int STAGES = 8;                    // X + packed-weight ring (memory latency)
     static constexpr int BSLOTS = 3;                    // B operand ring (transform -> MMA)
     static constexpr int XFORM_WARPS = 16;
     static constexpr int XFORM_GROUPS = 2;              // groups of warps on alternate stages
     static constexpr int GROUP_WARPS = XFORM_WARPS / XFORM_GROUPS;
     static constexpr int THREADS = 32 * (2 + XFORM_WARPS);  // producer, MMA, transform/epilogue
-    static constexpr int TMEM_COLS = 256;
+    static constexpr int TMEM_COLS = 128;
     static constexpr int MAX_SLICE_GROUPS = 64;         // K groups per quarter: K <= 32768
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * BSLOTS + 2;
     static constexpr int BAR_BYTES = 256;
@@ -268,10 +268,8 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
                 break;
             }
             const uint4 wv = *reinterpret_cast<const uint4*>(sW + s * Cfg::W_BYTES + r * 32 + q * 16);
-            const unsigned short sbits = sS[r * Cfg::MAX_SLICE_GROUPS + (i >> 1)];
-            const __half shi = __ushort_as_half(static_cast<unsigned short>(sbits & 0xFFF8u));
-            const __half slo = __float2half_rn(__half2float(__ushort_as_half(sbits)) - __half2float(shi));
-            const __half2 shi2 = __halves2half2(shi, shi), slo2 = __halves2half2(slo, slo);
+            const __half sc = __ushort_as_half(sS[r * Cfg::MAX_SLICE_GROUPS + (i >> 1)]);
+            const __half2 s2 = __halves2half2(sc, sc);
             uint8_t* bst = sB + b * Cfg::B_BYTES + bw;
             const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
@@ -280,38 +278,34 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
                 dequant_word_fast(words[h], pr);  // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
                 const uint32_t nat[4] = {__byte_perm(pr[0], pr[1], 0x5410), __byte_perm(pr[2], pr[3], 0x5410),
                                          __byte_perm(pr[0], pr[1], 0x7632), __byte_perm(pr[2], pr[3], 0x7632)};
-                uint32_t hi[4], lo[4];
+                uint32_t w[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const __half2 qv = *reinterpret_cast<const __half2*>(&nat[j]);
-                    __half2 a = __hmul2(qv, shi2), c = __hmul2(qv, slo2);
-                    hi[j] = *reinterpret_cast<uint32_t*>(&a);
-                    lo[j] = *reinterpret_cast<uint32_t*>(&c);
+                    __half2 a = __hmul2(qv, s2);  // q * s, rounded to fp16
+                    w[j] = *reinterpret_cast<uint32_t*>(&a);
                 }
                 const int c = 4 * q + h;                   // 16-byte chunk: k = 8c .. 8c + 7
                 const uint32_t off = static_cast<uint32_t>((c ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                // row 128 + r: sixteen atoms further, same swizzle phase
-                *reinterpret_cast<uint4*>(bst + 16 * 1024 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4*>(bst + off) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(ready_bar(b));
         }
-        // partial tile: TMEM lanes 32 (warp % 4) .. + 32, columns [32 ch, 32 ch + 32)
-        // (hi) and [128 + 32 ch, ...) (lo), added and stored to shared memory
+        // partial tile: TMEM lanes 32 (warp % 4) .. + 32, columns [32 ch, 32 ch + 32),
+        // stored to shared memory
         const bool got = bounded_wait(accf_bar, 0u, nullptr, p.ctl, kSiteW16TcAcc);
         const int quad = warp & 3, ch = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::XFORM_WARPS) : "memory");  // stages no longer read
         const bool have = ok && __all_sync(0xffffffffu, got) && !*abort_flag && num_kb > 0;
-        uint32_t vh[32], vl[32];
+        uint32_t vh[32];
         if (have) {
             tc_fence_after();
             const uint32_t ta = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                 static_cast<uint32_t>(32 * ch);
             tmem_ld_32x32b_x32(ta, vh);
-            tmem_ld_32x32b_x32(ta + 128u, vl);
             tmem_wait_ld();
         }
         float* dst = red + row * Cfg::RED_STRIDE + 32 * ch;
@@ -319,10 +313,8 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
         for (int j = 0; j < 32; j += 4) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (have)
-                v = make_float4(__uint_as_float(vh[j]) + __uint_as_float(vl[j]),
-                                __uint_as_float(vh[j + 1]) + __uint_as_float(vl[j + 1]),
-                                __uint_as_float(vh[j + 2]) + __uint_as_float(vl[j + 2]),
-                                __uint_as_float(vh[j + 3]) + __uint_as_float(vl[j + 3]));
+                v = make_float4(__uint_as_float(vh[j]), __uint_as_float(vh[j + 1]), __uint_as_float(vh[j + 2]),
+                                __uint_as_float(vh[j + 3]));
             *reinterpret_cast<float4*>(dst + j) = v;
         }
         fence_proxy_async_smem();  // the bulk copies read these rows

@@ -283,7 +283,11 @@ int gemm_f16(int64_t M, int64_t N, int64_t K,
  *  Wscale : fp16, N x (K/group), contiguous.  No zero points.
  *  group  : 128 (the only group size this build supports).
  *  Y      : fp16, M x N row-major, ldy >= N.
- *  K      : multiple of `group`.  No workspace. */
+ *  K      : multiple of `group`.  No workspace.
+ * Batches of up to 16 rows keep every weight exact (q applied as an exact
+ * fp16 integer, the scale in fp32 per group).  Larger batches on the tensor
+ * cores dequantize each weight to the fp16 product q * s (rounded once, at
+ * most 2^-11 of the weight); |Wscale| must stay below 8188 there. */
 int w4a16_gemm(int64_t M, int64_t N, int64_t K,
                const uint16_t *X, int64_t ldx,
                const uint8_t *Wq, const uint16_t *Wscale, int64_t group,
