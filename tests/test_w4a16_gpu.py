@@ -110,3 +110,12 @@ def test_w4a16_chain_reads_previous_output(dev, oracle, pdl, M):
     for w, s in layers:
         ref = oracle.w4a16(ref, w, s, GROUP).astype(np.float16)
     assert_fp16_close(got, ref.astype(np.float64), f"w4a16 chain M={M} pdl={pdl}")
+
+
+@pytest.mark.parametrize("M,N,K", [(9, 1000, 4608), (16, 300, 2048), (11, 4096, 4096), (16, 152, 128),
+                                   (14, 5000, 1024), (10, 33, 3968)])
+def test_w4a16_batched_gemv_shapes(dev, oracle, M, N, K):
+    """9 <= M <= 16: ragged N, unrolled and generic group loops, one and two
+    m16 tiles per CTA."""
+    X, Wq, S = _operands(M, N, K, idx=M + 3 * N)
+    assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), f"w4a16 {M}x{N}x{K}")
