@@ -117,11 +117,12 @@ def env_rank():
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples (200 ms) while the timed region runs."""
+    """nvidia-smi clock/throttle samples (every 50 ms); stop(t0, t1) keeps the
+    samples taken inside the timed region [t0, t1] (time.time() seconds)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -133,7 +134,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -145,7 +146,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp: str):
+        """Seconds since the epoch of an nvidia-smi timestamp (local time)."""
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0: float | None = None, t1: float | None = None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -155,23 +167,24 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((self._when(parts[9]), float(parts[1]), float(parts[2]),
+                             {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if t0 is not None and r[0] is not None and t0 <= r[0] <= t1]
+        use = inside if inside else rows
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(set().union(*(r[3] for r in use))) if use else [],
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "sampling_ms": 50}
 
 
 # --------------------------------------------------------------- workload
@@ -345,14 +358,16 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     t0 = time.perf_counter()
+    w0 = time.time()
     launches = 0
     for i in range(args.steps):
         launches += step(i)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    w1 = time.time()
     if dist:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(w0, w1)
     assert qg.device_status() == qg.QG_OK, "device-side wait timed out in the timed region"
 
     t_op = {op: [a.elapsed_time(b) for a, b in ev[op]] for op in OPS}          # ms
@@ -518,15 +533,20 @@ def measure_e2e(wl, args):
                   "conversion + GEMM and copy-out overlapped on the library's three streams)"}
 
 
-def oracle_baseline(seconds: float, rows: int | None = None):
-    """The CPU oracle on a bounded sample of the INT8 GEMM: `rows` rows of
-    C = A . B^T at N = K = 8192, timed on the host cores."""
-    import oracle
+def oracle_operands():
+    """The seeded 8192^3 INT8 operands of the headline GEMM (host arrays)."""
     from bit_quantized_tensor_gb300 import inputs
+    return inputs.s8_uniform(N_SQ, N_SQ, 1002), inputs.s8_uniform(N_SQ, N_SQ, 2002)
+
+
+def oracle_baseline(seconds: float, rows: int | None = None, operands=None):
+    """The CPU oracle on a bounded sample of the INT8 GEMM: `rows` rows of
+    C = A . B^T at N = K = 8192 (sized to about `seconds` when None), timed on
+    the host cores."""
+    import oracle
     oracle.build()
     n = N_SQ
-    A = inputs.s8_uniform(n, n, 1002)
-    B = inputs.s8_uniform(n, n, 2002)
+    A, B = operands if operands is not None else oracle_operands()
     cores = oracle.threads()
     if rows is None:
         probe = max(cores, 4)
@@ -539,7 +559,7 @@ def oracle_baseline(seconds: float, rows: int | None = None):
     oracle.gemm_s8(A[:rows], B)
     dt = time.perf_counter() - t0
     return {"value": round(2.0 * rows * n * n / dt / 1e12, 6), "unit": "TOPS", "cores": cores,
-            "kind": "oracle", "seconds": round(dt, 2),
+            "kind": "oracle", "seconds": round(dt, 2), "rows": rows,
             "sample": f"{rows} rows of the 8192^3 INT8 GEMM (C[rows] = A[rows] . B^T, int64 "
                       f"accumulation), {cores} threads"}
 
@@ -550,12 +570,15 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
+    ops = oracle_operands()
+    # one sample size for every step: about cpu_seconds for the whole run
+    rows = oracle_baseline(args.cpu_seconds / max(args.steps, 1), operands=ops)["rows"]
     for _ in range(max(args.warmup, 0)):
-        oracle_baseline(0.5)
+        oracle_baseline(0.0, rows=rows, operands=ops)
     vals, t0 = [], time.perf_counter()
     last = None
     for _ in range(args.steps):
-        last = oracle_baseline(args.cpu_seconds / max(args.steps, 1))
+        last = oracle_baseline(0.0, rows=rows, operands=ops)
         vals.append(last["value"])
     wall = time.perf_counter() - t0
     value = round(statistics.median(vals), 6)
@@ -576,7 +599,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
