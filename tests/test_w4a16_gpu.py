@@ -119,3 +119,38 @@ def test_w4a16_batched_gemv_shapes(dev, oracle, M, N, K):
     m16 tiles per CTA."""
     X, Wq, S = _operands(M, N, K, idx=M + 3 * N)
     assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), f"w4a16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 8192), (1, 4096, 11008), (4, 4096, 8192), (8, 4096, 4096),
+                                   (1, 3000, 16384), (2, 4100, 8320)])
+def test_w4a16_gemv_large_slabs(dev, oracle, M, N, K):
+    """Decode shapes whose weight slab per SM does not fit at half an SM
+    (fewer rows per CTA, more CTAs than SMs)."""
+    X, Wq, S = _operands(M, N, K, idx=M + 7 * N)
+    assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), f"w4a16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("pdl", [1, 0])
+def test_w4a16_chain_of_large_layers(dev, oracle, pdl):
+    """A chain of N = K = 8192 decode layers (M = 1, more CTAs than SMs): each
+    call reads X only after the previous call has finished."""
+    import torch
+    import bit_quantized_tensor_gb300 as qg
+    N = K = 8192
+    layers = [(inputs.s4_packed_uniform(N, K, 2400 + i),
+               inputs.f16_uniform(N, K // GROUP, 0.0035, 0.0055, 3400 + i)) for i in range(3)]
+    X0 = inputs.f16_normal(1, K, 1400)
+    qg.lib().qg_set_pdl(pdl)
+    try:
+        x = _t(X0, dev)
+        dW = [(_t(w, dev), _t(s, dev)) for w, s in layers]
+        for w, s in dW:
+            x = qg.w4a16_gemm(x, w, s, GROUP)
+        torch.cuda.synchronize()
+        got = x.cpu().numpy()
+    finally:
+        qg.lib().qg_set_pdl(1)
+    ref = X0
+    for w, s in layers:
+        ref = oracle.w4a16(ref, w, s, GROUP).astype(np.float16)
+    assert_fp16_close(got, ref.astype(np.float64), f"w4a16 large chain pdl={pdl}")
