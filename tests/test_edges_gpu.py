@@ -8,6 +8,9 @@
   sentinel pattern, with a row stride larger than N; after the call the rows
   above and below and the columns past N must still hold the sentinel, and
   the view must match the oracle.
+- Strided inputs: every input that takes a leading dimension is read as the
+  first K columns of a wider buffer (whose extra columns hold values that
+  would change the result if they were read).
 """
 import numpy as np
 import pytest
@@ -208,3 +211,67 @@ def test_w4a4_gemm_writes_only_its_output(dev, oracle, gemm_path, path):
     _check_guards(buf, M, N)
     ref = oracle.w4a4_gemm(qx, sx, qw, sw, BLOCK, K, XU=xu16.astype(np.float64), V=V, bias=b)
     assert_fp16_close(Y.cpu().numpy(), ref, "w4a4 guarded")
+
+
+# ---------------------------------------------------------- strided inputs
+
+def _wide(a, extra, fill):
+    """a as the left columns of a wider array whose other columns hold `fill`."""
+    w = np.full((a.shape[0], a.shape[1] + extra), fill, dtype=a.dtype)
+    w[:, :a.shape[1]] = a
+    return w
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_gemms_read_inputs_through_leading_dimensions(dev, oracle, gemm_path, path):
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    M, N, K = 300, 520, 1104
+    A = inputs.s8_uniform(M, K, 4100)
+    B = inputs.s8_uniform(N, K, 4101)
+    tA, tB = _t(_wide(A, 48, 127), dev)[:, :K], _t(_wide(B, 32, -128), dev)[:, :K]
+    assert tA.stride(0) == K + 48 and tB.stride(0) == K + 32
+    C = qg.qgemm_s8(tA, tB).cpu().numpy()
+    ref = oracle.gemm_s8(A, B)
+    assert np.array_equal(C, ref), first_mismatch(C, ref)
+
+    K4 = 1088  # a multiple of 32; rows of 544 bytes, strides of 560 and 592
+    A4 = inputs.s4_packed_uniform(M, K4, 4102)
+    B4 = inputs.s4_packed_uniform(N, K4, 4103)
+    tA4 = _t(_wide(A4, 16, 0x77), dev)[:, :K4 // 2]
+    tB4 = _t(_wide(B4, 48, 0x88), dev)[:, :K4 // 2]
+    C4 = qg.qgemm_s4(tA4, tB4, K4).cpu().numpy()
+    ref4 = oracle.gemm_s4(A4, B4, K4)
+    assert np.array_equal(C4, ref4), first_mismatch(C4, ref4)
+
+    Af = inputs.f16_normal(M, K, 4104)
+    Bf = inputs.f16_normal(N, K, 4105)
+    Cf = qg.gemm_f16(_t(_wide(Af, 8, np.float16(1000)), dev)[:, :K],
+                     _t(_wide(Bf, 24, np.float16(-1000)), dev)[:, :K]).cpu().numpy()
+    assert_fp16_close(Cf, oracle.gemm_f16(Af, Bf), "gemm_f16 strided inputs")
+
+
+@pytest.mark.parametrize("M", [1, 12, 40])
+def test_w4a16_reads_x_through_its_leading_dimension(dev, oracle, M):
+    """Decode GEMV (M=1), batched GEMV (M=12) and the tensor-core path (M=40)."""
+    import bit_quantized_tensor_gb300 as qg
+    N, K = 700, 1024
+    X = inputs.f16_normal(M, K, 4110 + M)
+    Wq = inputs.s4_packed_uniform(N, K, 4120 + M)
+    S = inputs.f16_uniform(N, K // GROUP, 0.005, 0.02, 4130 + M)
+    tX = _t(_wide(X, 64, np.float16(500)), dev)[:, :K]
+    assert tX.stride(0) == K + 64
+    Y = qg.w4a16_gemm(tX, _t(Wq, dev), _t(S, dev), GROUP).cpu().numpy()
+    assert_fp16_close(Y, oracle.w4a16(X, Wq, S, GROUP), f"w4a16 strided X M={M}")
+
+
+def test_w4a4_quantize_reads_x_through_its_leading_dimension(dev, oracle):
+    import bit_quantized_tensor_gb300 as qg
+    M, K = 70, 576
+    X = inputs.f32_normal(M, K, 4140)
+    tX = _t(_wide(X, 20, np.float32(1e6)), dev)[:, :K]
+    assert tX.stride(0) == K + 20
+    q, sc, _ = qg.w4a4_quantize(tX, None, BLOCK)
+    q_ref, s_ref = oracle.w4a4_quantize(X, BLOCK)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sc.cpu().numpy().view(np.uint16), s_ref)
