@@ -31,6 +31,9 @@ _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
 
 
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/liboracle.so`` (gcc, no fast-math)."""
     with _lock:
@@ -38,8 +41,7 @@ def build(force: bool = False) -> str:
                 and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
             return _LIB
         tmp = _LIB + ".tmp%d" % os.getpid()
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
-               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+        cmd = ["gcc"] + CFLAGS + [_SRC, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
         return _LIB
@@ -48,7 +50,10 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        # ORACLE_LIB_PATH: a build of a modified copy of the source, loaded
+        # instead (the mutation test plants one mistake per build and checks
+        # that the pins catch it)
+        lib = ctypes.CDLL(os.environ.get("ORACLE_LIB_PATH") or build())
         sig = {
             "orc_half_to_double": (ctypes.c_double, [ctypes.c_uint16]),
             "orc_float_to_half": (ctypes.c_uint16, [ctypes.c_float]),
