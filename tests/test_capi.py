@@ -1,5 +1,7 @@
 """CPU checks of the C ABI: the library loads, exports every declared symbol,
 and rejects bad arguments synchronously (before touching any GPU)."""
+import os
+
 import pytest
 
 import bit_quantized_tensor_gb300 as qg
@@ -142,3 +144,34 @@ def test_knob_ranges(L):
         assert L.qg_set_l2_policy(m) == 0
     assert L.qg_set_gemm_path(3) == 1 and L.qg_set_gemm_path(0) == 0
     assert L.qg_set_s8_chunk(0) == 1 and L.qg_set_s8_chunk(17) == 1 and L.qg_set_s8_chunk(16) == 0
+
+
+def test_product_package_never_touches_the_oracle():
+    """The library's Python package and its C sources name no part of the
+    CPU oracle: the product path has no CPU fallback to reach."""
+    import re
+    pkg = os.path.dirname(qg.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert not re.search(r"\boracle\b|liboracle|qgemm_oracle", text), f
+
+
+def test_binding_raises_without_its_library(tmp_path):
+    """With the shared library absent the binding refuses to run (it does not
+    fall back to anything)."""
+    import subprocess
+    import sys
+    code = ("import bit_quantized_tensor_gb300 as qg\n"
+            f"qg.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+            "qg._lib = None\n"
+            "try:\n"
+            "    qg.lib()\n"
+            "except Exception as e:\n"
+            "    print('raised', type(e).__name__)\n"
+            "else:\n"
+            "    print('loaded')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(os.path.dirname(__file__)),
+                       capture_output=True, text=True, timeout=300)
+    assert r.stdout.strip().startswith("raised"), r.stdout + r.stderr
