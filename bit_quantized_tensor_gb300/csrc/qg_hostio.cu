@@ -182,35 +182,51 @@ extern "C" int qgemm_s8_host(int64_t M, int64_t N, int64_t K, const int8_t* A, i
                                   q->in);
         if (e == cudaSuccess) e = cudaEventRecord(ev_b[j], q->in);
     };
-    copy_a(0);
-    for (int j = 0; j < p.b; ++j) copy_b(j);
-    for (int i = 1; i < p.a; ++i) copy_a(i);
+    // Copy-in order A0, B0, A1, B1, A2, ...: the first pieces need only the
+    // first slices, and the first rows of C start back across the link early
+    // (with all of B first, the second row of pieces waited behind it).
+    const int nin = p.a > p.b ? p.a : p.b;
+    for (int k = 0; k < nin; ++k) {
+        if (k < p.a) copy_a(k);
+        if (k < p.b) copy_b(k);
+    }
 
-    // compute and copy-out, piece by piece
-    for (int i = 0; i < p.a && e == cudaSuccess && rc == QG_OK; ++i) {
+    // One piece: convert its slices on first use, GEMM, copy the piece of C out.
+    bool a_conv[kMaxASlices] = {}, b_conv[kMaxBSlices] = {};
+    auto piece = [&](int i, int j) {
         const int64_t r0 = static_cast<int64_t>(i) * p.ra;
-        for (int j = 0; j < p.b && e == cudaSuccess && rc == QG_OK; ++j) {
-            const int64_t c0 = static_cast<int64_t>(j) * p.cb;
-            if (j == 0) {
-                e = cudaStreamWaitEvent(q->comp, ev_a[i], 0);
-                if (e == cudaSuccess) rc = qg::s8_to_f16_rows(d.a8 + r0 * K, rows_a(i), K, d.a16 + r0 * K, K, dev, q->comp);
-            }
-            if (i == 0 && e == cudaSuccess && rc == QG_OK) {
-                e = cudaStreamWaitEvent(q->comp, ev_b[j], 0);
-                if (e == cudaSuccess) rc = qg::s8_to_f16_rows(d.b8 + c0 * K, rows_b(j), K, d.b16 + c0 * K, K, dev, q->comp);
-            }
-            if (e != cudaSuccess || rc != QG_OK) break;
-            rc = qg::run_gemm_s8_converted(d.a16 + r0 * K, d.b16 + c0 * K, rows_a(i), rows_b(j), K,
-                                           d.c32 + r0 * d.ldc32 + c0, d.ldc32, ctl, q->comp);
-            if (rc != QG_OK) break;
-            cudaEvent_t ev = ev_piece[i * kMaxBSlices + j];
-            e = cudaEventRecord(ev, q->comp);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(q->out, ev, 0);
-            if (e == cudaSuccess)
-                e = cudaMemcpy2DAsync(C + r0 * ldc + c0, static_cast<size_t>(ldc) * 4, d.c32 + r0 * d.ldc32 + c0,
-                                      static_cast<size_t>(d.ldc32) * 4, static_cast<size_t>(rows_b(j)) * 4,
-                                      static_cast<size_t>(rows_a(i)), cudaMemcpyDeviceToHost, q->out);
+        const int64_t c0 = static_cast<int64_t>(j) * p.cb;
+        if (!a_conv[i]) {
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(q->comp, ev_a[i], 0);
+            if (e == cudaSuccess && rc == QG_OK)
+                rc = qg::s8_to_f16_rows(d.a8 + r0 * K, rows_a(i), K, d.a16 + r0 * K, K, dev, q->comp);
+            a_conv[i] = true;
         }
+        if (!b_conv[j]) {
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(q->comp, ev_b[j], 0);
+            if (e == cudaSuccess && rc == QG_OK)
+                rc = qg::s8_to_f16_rows(d.b8 + c0 * K, rows_b(j), K, d.b16 + c0 * K, K, dev, q->comp);
+            b_conv[j] = true;
+        }
+        if (e != cudaSuccess || rc != QG_OK) return;
+        rc = qg::run_gemm_s8_converted(d.a16 + r0 * K, d.b16 + c0 * K, rows_a(i), rows_b(j), K,
+                                       d.c32 + r0 * d.ldc32 + c0, d.ldc32, ctl, q->comp);
+        if (rc != QG_OK) return;
+        cudaEvent_t ev = ev_piece[i * kMaxBSlices + j];
+        e = cudaEventRecord(ev, q->comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(q->out, ev, 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(C + r0 * ldc + c0, static_cast<size_t>(ldc) * 4, d.c32 + r0 * d.ldc32 + c0,
+                                  static_cast<size_t>(d.ldc32) * 4, static_cast<size_t>(rows_b(j)) * 4,
+                                  static_cast<size_t>(rows_a(i)), cudaMemcpyDeviceToHost, q->out);
+    };
+    // Pieces in the order their slices arrive: each slice, once copied in,
+    // completes the pieces whose other slice is already there.
+    for (int k = 0; k < nin && e == cudaSuccess && rc == QG_OK; ++k) {
+        if (k < p.a)
+            for (int j = 0; j < p.b && j < k && e == cudaSuccess && rc == QG_OK; ++j) piece(k, j);
+        if (k < p.b)
+            for (int i = 0; i < p.a && i <= k && e == cudaSuccess && rc == QG_OK; ++i) piece(i, k);
     }
     if (e == cudaSuccess && rc == QG_OK) {
         // join all three queues back into the caller's stream (the copy-out
