@@ -34,7 +34,8 @@ STATUS_NAMES = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED",
                 3: "QG_ERR_MISALIGNED", 4: "QG_ERR_WORKSPACE", 5: "QG_ERR_CUDA",
                 6: "QG_ERR_TIMEOUT"}
 QG_ROW_MAJOR, QG_COL_MAJOR = 0, 1
-QG_OP_S8, QG_OP_S4, QG_OP_F16, QG_OP_W4A16, QG_OP_W4A4, QG_OP_S8_HOST = range(6)
+(QG_OP_S8, QG_OP_S4, QG_OP_F16, QG_OP_W4A16, QG_OP_W4A4, QG_OP_S8_HOST, QG_OP_W4A4_PREPACKED,
+ QG_OP_W4A4_WEIGHTS) = range(8)
 
 
 class QgError(RuntimeError):
@@ -84,6 +85,9 @@ SIGNATURES = {
                          _p, _sz, _p]),
     "w4a4_gemm_affine": (_int, [_i64, _i64, _i64, _p, _p, _p, _p, _i64, _p, _p, _i64, _p, _p, _p,
                                 _i64, _p, _sz, _p]),
+    "w4a4_prepack_weights": (_int, [_i64, _i64, _p, _p, _i64, _p, _p, _sz, _p]),
+    "w4a4_gemm_prepacked": (_int, [_i64, _i64, _i64, _p, _p, _p, _sz, _i64, _p, _p, _i64, _p, _p, _i64,
+                                   _p, _sz, _p]),
 }
 
 _lib = None
@@ -375,4 +379,54 @@ def w4a4_gemm(Xq, Xscale, Wq, Wscale, K: int, XU=None, Vt=None, bias=None, block
         _check("w4a4_gemm", lib().w4a4_gemm(*head, *tail))
     else:
         _check("w4a4_gemm_affine", lib().w4a4_gemm_affine(*head, alpha.data_ptr(), *tail))
+    return Y
+
+
+def w4a4_prepack_weights(Wq, Wscale, K: int, alpha=None, block: int = 64, out=None, stream=None):
+    """The weight side of w4a4_gemm prepared once: a uint8 device buffer for
+    w4a4_gemm_prepacked (with the column multiplier alpha folded in, if given)."""
+    torch = _torch()
+    _cuda(Wq, torch.uint8, "Wq")
+    _cuda(Wscale, torch.float16, "Wscale")
+    N = Wq.shape[0]
+    if alpha is not None:
+        _cuda(alpha, torch.float16, "alpha")
+        if alpha.numel() != N:
+            raise ValueError("alpha must hold N fp16 column multipliers")
+    nbytes = workspace_size(QG_OP_W4A4_WEIGHTS, 1, N, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=Wq.device)
+    _check("w4a4_prepack_weights", lib().w4a4_prepack_weights(
+        N, K, Wq.data_ptr(), Wscale.data_ptr(), block,
+        alpha.data_ptr() if alpha is not None else None, out.data_ptr(), out.numel(), _stream(stream)))
+    return out
+
+
+def w4a4_gemm_prepacked(Xq, Xscale, packed, N: int, K: int, XU=None, Vt=None, bias=None, block: int = 64,
+                        Y=None, ws=None, stream=None):
+    """w4a4_gemm with weights from w4a4_prepack_weights (only X is converted per call)."""
+    torch = _torch()
+    _cuda(Xq, torch.uint8, "Xq")
+    _cuda(Xscale, torch.float16, "Xscale")
+    _cuda(packed, torch.uint8, "packed")
+    M = Xq.shape[0]
+    rank = 0
+    V = Vt
+    if XU is not None:
+        _cuda(XU, torch.float16, "XU")
+        _cuda(V, torch.float16, "Vt")
+        rank = XU.shape[1]
+        if not V.is_contiguous() or V.dim() != 2 or V.shape != (N, rank):
+            raise ValueError("Vt must be a contiguous N x rank fp16 matrix")
+    if bias is not None:
+        _cuda(bias, torch.float16, "bias")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=Xq.device)
+    _cuda(Y, torch.float16, "Y")
+    ws, wsb = _workspace(QG_OP_W4A4_PREPACKED, M, N, K, Xq.device, ws)
+    _check("w4a4_gemm_prepacked", lib().w4a4_gemm_prepacked(
+        M, N, K, Xq.data_ptr(), Xscale.data_ptr(), packed.data_ptr(), packed.numel(), block,
+        XU.data_ptr() if rank else None, V.data_ptr() if rank else None, rank,
+        bias.data_ptr() if bias is not None else None, Y.data_ptr(), Y.stride(0),
+        ws.data_ptr(), wsb, _stream(stream)))
     return Y

@@ -129,6 +129,16 @@ size_t qg_workspace_size(int op, int64_t M, int64_t N, int64_t K) {
             return round_up256(m * k) + round_up256(n * k) + round_up256(4 * nblk * mp) +
                    round_up256(4 * nblk * np);
         }
+        case QG_OP_W4A4_PREPACKED: {  // the X side only
+            const size_t nblk = k / 64 + 1;
+            const size_t mp = (m + 3) & ~static_cast<size_t>(3);
+            return round_up256(m * k) + round_up256(4 * nblk * mp);
+        }
+        case QG_OP_W4A4_WEIGHTS: {  // packed weights: e4m3 codes, transposed scale table (M unused)
+            const size_t nblk = k / 64 + 1;
+            const size_t np = (n + 3) & ~static_cast<size_t>(3);
+            return round_up256(n * k) + round_up256(4 * nblk * np);
+        }
         default:
             return 0;
     }

@@ -370,6 +370,12 @@ int s4_to_e4m3_pair(const uint8_t* a, int64_t a_rows, int64_t a_lds, uint8_t* a_
     return launch_expand<S4ToE4M3>(jobs, 2, K / 32, dev, s);
 }
 
+int s4_to_e4m3_rows(const uint8_t* src, int64_t rows, int64_t lds, uint8_t* dst, int64_t K, int dev,
+                    cudaStream_t s) {
+    const ExpandJob job = {src, rows, lds, dst, K};
+    return launch_expand<S4ToE4M3>(&job, 1, K / 32, dev, s);
+}
+
 int conv_grid(int dev, int64_t work_items) {
     const int64_t per_block = 256;
     int64_t g = (work_items + per_block - 1) / per_block;

@@ -50,6 +50,11 @@ int conv_grid(int dev, int64_t work_items);
 // Packed signed 4-bit rows (K values, low nibble = even k) of two operands
 // -> one e4m3 byte per value (exact, destination row stride K bytes), one
 // launch enqueued on `s`.  K is a multiple of 32.
+// One operand of s4_to_e4m3_pair: rows of packed nibbles (row stride lds
+// bytes) -> rows of K e4m3 bytes.
+int s4_to_e4m3_rows(const uint8_t* src, int64_t rows, int64_t lds, uint8_t* dst, int64_t K, int dev,
+                    cudaStream_t s);
+
 int s4_to_e4m3_pair(const uint8_t* a, int64_t a_rows, int64_t a_lds, uint8_t* a_dst, const uint8_t* b,
                     int64_t b_rows, int64_t b_lds, uint8_t* b_dst, int64_t K, int dev, cudaStream_t s);
 

@@ -481,6 +481,30 @@ int w4a4_quantize(int64_t M, int64_t K, const float* X, int64_t ldx, const uint1
 
 namespace qg {
 
+// The GEMM on converted operands: A8 / B8 e4m3 codes (M x K, N x K), SXt /
+// SWt the transposed fp32 scale tables (K/64 + 1 rows of Mp / Np floats).
+static int w4a4_run(int64_t M, int64_t N, int64_t K, const uint8_t* A8, const float* SXt, const uint8_t* B8,
+                    const float* SWt, const uint16_t* XU, const uint16_t* V, int64_t rank, const uint16_t* bias,
+                    uint16_t* Y, int64_t ldy, const Ctl& ctl, int dev, cudaStream_t s) {
+    const int nblk = static_cast<int>(K / kW4A4Block);
+    const int64_t Mp = (M + 3) & ~int64_t(3), Np = (N + 3) & ~int64_t(3);
+    W4A4Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_ks = static_cast<int>((K + W4A4Cfg::BK - 1) / W4A4Cfg::BK);
+    p.nblk = nblk;
+    p.lowrank = rank ? 1 : 0;
+    p.Y = reinterpret_cast<__half*>(Y);
+    p.ldy = ldy;
+    p.bias = reinterpret_cast<const __half*>(bias);
+    p.ctl = ctl;
+    const int path = gemm_path();
+    const bool pairs = path == 2 || (path == 0 && M > W4A4Cfg::BM);
+    return pairs ? launch_w4a4<W4A4PairCfg, true>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s)
+                 : launch_w4a4<W4A4Cfg, false>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s);
+}
+
 // w4a4_gemm and w4a4_gemm_affine: alpha == nullptr is the formula as printed.
 static int w4a4_gemm_impl(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
                           const uint8_t* Wq, const uint16_t* Wscale, int64_t block, const uint16_t* XU,
@@ -523,22 +547,13 @@ static int w4a4_gemm_impl(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, co
         SWt);
     rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
+    return w4a4_run(M, N, K, A8, SXt, B8, SWt, XU, V, rank, bias, Y, ldy, ctl, dev, s);
+}
 
-    W4A4Params p;
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.num_ks = static_cast<int>((K + W4A4Cfg::BK - 1) / W4A4Cfg::BK);
-    p.nblk = nblk;
-    p.lowrank = rank ? 1 : 0;
-    p.Y = reinterpret_cast<__half*>(Y);
-    p.ldy = ldy;
-    p.bias = reinterpret_cast<const __half*>(bias);
-    p.ctl = ctl;
-    const int path = gemm_path();
-    const bool pairs = path == 2 || (path == 0 && M > W4A4Cfg::BM);
-    return pairs ? launch_w4a4<W4A4PairCfg, true>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s)
-                 : launch_w4a4<W4A4Cfg, false>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s);
+// Offset of the scale table inside a buffer of packed weights (after the
+// e4m3 codes, N x K bytes).
+static size_t w4a4_packed_scales_offset(int64_t N, int64_t K) {
+    return (static_cast<size_t>(N) * static_cast<size_t>(K) + 255) & ~static_cast<size_t>(255);
 }
 
 }  // namespace qg
@@ -562,6 +577,67 @@ int w4a4_gemm_affine(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const u
     if (!alpha) return QG_ERR_INVALID_ARG;
     return w4a4_gemm_impl(M, N, K, Xq, Xscale, Wq, Wscale, block, XU, V, rank, alpha, bias, Y, ldy,
                           ws, ws_bytes, stream);
+}
+
+int w4a4_prepack_weights(int64_t N, int64_t K, const uint8_t* Wq, const uint16_t* Wscale, int64_t block,
+                         const uint16_t* alpha, void* packed, size_t packed_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_prepack_weights");
+    if (N < 1 || K < 1 || N > INT32_MAX || K > INT32_MAX) return QG_ERR_INVALID_ARG;
+    if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;
+    if (K % kW4A4Block) return QG_ERR_INVALID_ARG;
+    if (!Wq || !Wscale || !packed) return QG_ERR_INVALID_ARG;
+    if (!aligned16(Wq) || (reinterpret_cast<uintptr_t>(packed) & 255u)) return QG_ERR_MISALIGNED;
+    if (packed_bytes < qg_workspace_size(QG_OP_W4A4_WEIGHTS, 1, N, K)) return QG_ERR_WORKSPACE;
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int nblk = static_cast<int>(K / kW4A4Block);
+    const int64_t Np = (N + 3) & ~int64_t(3);
+    uint8_t* B8 = static_cast<uint8_t*>(packed);
+    float* SWt = reinterpret_cast<float*>(B8 + w4a4_packed_scales_offset(N, K));
+    int rc = s4_to_e4m3_rows(Wq, N, K / 2, B8, K, dev, s);
+    if (rc) return rc;
+    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
+        N, Np, nblk, reinterpret_cast<const __half*>(Wscale), reinterpret_cast<const __half*>(alpha), SWt);
+    return map_cuda(cudaGetLastError());
+}
+
+int w4a4_gemm_prepacked(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, const uint16_t* Xscale,
+                        const void* packed, size_t packed_bytes, int64_t block, const uint16_t* XU,
+                        const uint16_t* V, int64_t rank, const uint16_t* bias, uint16_t* Y, int64_t ldy,
+                        void* ws, size_t ws_bytes, void* stream) {
+    const qg::NvtxRange nvtx_range("w4a4_gemm_prepacked");
+    if (M < 1 || N < 1 || K < 1 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return QG_ERR_INVALID_ARG;
+    if (block != kW4A4Block) return QG_ERR_UNSUPPORTED;
+    if (K % kW4A4Block) return QG_ERR_INVALID_ARG;
+    if (rank != 0 && rank != kW4A4MaxRank) return QG_ERR_UNSUPPORTED;
+    if (!Xq || !Xscale || !packed || !Y || (rank && (!XU || !V))) return QG_ERR_INVALID_ARG;
+    if (ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(Xq) || !aligned16(Y) || (rank && (!aligned16(XU) || !aligned16(V))) ||
+        (reinterpret_cast<uintptr_t>(packed) & 255u))
+        return QG_ERR_MISALIGNED;
+    if (packed_bytes < qg_workspace_size(QG_OP_W4A4_WEIGHTS, 1, N, K)) return QG_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < qg_workspace_size(QG_OP_W4A4_PREPACKED, M, N, K)) return QG_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return QG_ERR_MISALIGNED;
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    Ctl ctl = host_ctl(dev);
+    if (!ctl.status) return QG_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int nblk = static_cast<int>(K / kW4A4Block);
+    const int64_t Mp = (M + 3) & ~int64_t(3);
+    uint8_t* A8 = static_cast<uint8_t*>(ws);
+    float* SXt = reinterpret_cast<float*>(A8 + ((static_cast<size_t>(M) * K + 255) & ~static_cast<size_t>(255)));
+    int rc = s4_to_e4m3_rows(Xq, M, K / 2, A8, K, dev, s);
+    if (rc) return rc;
+    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
+        M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), nullptr, SXt);
+    rc = map_cuda(cudaGetLastError());
+    if (rc) return rc;
+    const uint8_t* B8 = static_cast<const uint8_t*>(packed);
+    const float* SWt = reinterpret_cast<const float*>(B8 + w4a4_packed_scales_offset(N, K));
+    return w4a4_run(M, N, K, A8, SXt, B8, SWt, XU, V, rank, bias, Y, ldy, ctl, dev, s);
 }
 
 }  // extern "C"

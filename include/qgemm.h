@@ -60,7 +60,9 @@ typedef enum { QG_ROW_MAJOR = 0, QG_COL_MAJOR = 1 } qg_layout;
 
 /* Operation ids for qg_workspace_size. */
 typedef enum {
-    QG_OP_S8 = 0, QG_OP_S4 = 1, QG_OP_F16 = 2, QG_OP_W4A16 = 3, QG_OP_W4A4 = 4, QG_OP_S8_HOST = 5
+    QG_OP_S8 = 0, QG_OP_S4 = 1, QG_OP_F16 = 2, QG_OP_W4A16 = 3, QG_OP_W4A4 = 4, QG_OP_S8_HOST = 5,
+    QG_OP_W4A4_PREPACKED = 6,  /* workspace of w4a4_gemm_prepacked */
+    QG_OP_W4A4_WEIGHTS = 7     /* size of the buffer w4a4_prepack_weights fills (M unused: pass 1) */
 } qg_op;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -355,6 +357,36 @@ int w4a4_gemm_affine(int64_t M, int64_t N, int64_t K,
                      const uint16_t *alpha, const uint16_t *bias,
                      uint16_t *Y, int64_t ldy,
                      void *ws, size_t ws_bytes, void *stream);
+
+/* [W4A4] The weight side of w4a4_gemm prepared once (the page's weights are
+ * quantized offline; inference reuses them for every call): writes into
+ * `packed` the e4m3 codes of Wq (N x K bytes) and the transposed fp32 table
+ * of Wscale (with the column multiplier alpha folded in when alpha is not
+ * NULL, as in w4a4_gemm_affine).
+ *  Wq, Wscale, block : as in w4a4_gemm (N rows).
+ *  alpha  : fp16 N column multipliers, or NULL (= 1).
+ *  packed : device buffer of qg_workspace_size(QG_OP_W4A4_WEIGHTS, 1, N, K)
+ *           bytes, 256-byte aligned, owned by the caller; valid once the
+ *           work on `stream` has run.  Its layout is private to this library.
+ * Errors as in w4a4_gemm. */
+int w4a4_prepack_weights(int64_t N, int64_t K, const uint8_t *Wq, const uint16_t *Wscale,
+                         int64_t block, const uint16_t *alpha,
+                         void *packed, size_t packed_bytes, void *stream);
+
+/* [W4A4] w4a4_gemm (or w4a4_gemm_affine, when alpha was given to
+ * w4a4_prepack_weights) with the weights from w4a4_prepack_weights: only X
+ * is converted per call.  The result is bit for bit that of w4a4_gemm on
+ * the same inputs (the same kernels on the same operands).
+ *  packed, packed_bytes : from w4a4_prepack_weights for these N, K.
+ *  ws : workspace of qg_workspace_size(QG_OP_W4A4_PREPACKED, M, N, K) bytes,
+ *       256-byte aligned.
+ * Every other argument as in w4a4_gemm. */
+int w4a4_gemm_prepacked(int64_t M, int64_t N, int64_t K,
+                        const uint8_t *Xq, const uint16_t *Xscale,
+                        const void *packed, size_t packed_bytes, int64_t block,
+                        const uint16_t *XU, const uint16_t *V, int64_t rank,
+                        const uint16_t *bias, uint16_t *Y, int64_t ldy,
+                        void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

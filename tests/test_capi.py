@@ -109,6 +109,17 @@ def test_w4a16_and_w4a4_argument_errors(L):
                               FAKE, 8, WS, big, None) == 2
     assert L.w4a4_gemm_affine(4, 8, 128, FAKE, FAKE, FAKE, FAKE, 64, None, None, 0, FAKE, None,
                               FAKE, 8, WS, 16, None) == 4
+    # w4a4_prepack_weights(N, K, Wq, Ws, block, alpha, packed, bytes, stream)
+    assert L.w4a4_prepack_weights(8, 128, FAKE, FAKE, 32, None, WS, big, None) == 2
+    assert L.w4a4_prepack_weights(8, 96, FAKE, FAKE, 64, None, WS, big, None) == 1
+    assert L.w4a4_prepack_weights(8, 128, FAKE, FAKE, 64, None, WS, 16, None) == 4
+    assert L.w4a4_prepack_weights(8, 128, FAKE, FAKE, 64, None, WS + 16, big, None) == 3
+    # w4a4_gemm_prepacked(M, N, K, Xq, Xs, packed, bytes, block, XU, V, rank, bias, Y, ldy, ws, wsb, stream)
+    assert L.w4a4_gemm_prepacked(4, 8, 128, FAKE, FAKE, WS, big, 64, None, None, 0, None, FAKE, 8,
+                                 WS, 16, None) == 4
+    assert L.w4a4_gemm_prepacked(4, 8, 128, FAKE, FAKE, WS, 16, 64, None, None, 0, None, FAKE, 8,
+                                 WS, big, None) == 1
+    assert L.qg_workspace_size(7, 1, 8, 128) < L.qg_workspace_size(4, 4, 8, 128)
 
 
 def _s8h(L, M=64, N=64, K=64, A=FAKE, lda=64, B=FAKE, ldb=64, C=FAKE, ldc=64, ws=WS, wsb=1 << 30):

@@ -234,6 +234,35 @@ def test_gemm_affine_unit_alpha_equals_plain_call(dev, oracle):
     assert np.array_equal(Y0.view(np.uint16), Y1.view(np.uint16))
 
 
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("M,N,K,rank,bias,affine", [(100, 300, 256, 32, True, False),
+                                                    (520, 392, 1088, 32, True, True),
+                                                    (129, 257, 576, 0, False, False)])
+def test_prepacked_weights_give_the_same_bits(dev, oracle, gemm_path, path, M, N, K, rank, bias, affine):
+    """w4a4_prepack_weights + w4a4_gemm_prepacked against w4a4_gemm (or
+    w4a4_gemm_affine) on the same inputs: the same bits, and the oracle."""
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    X, W, U, V, b = _gemm_case(M, N, K, 13, rank, bias)
+    alpha = inputs.f16_uniform(1, N, 0.5, 2.0, 3500 + M)[0] if affine else None
+    qx, sx, xu = qg.w4a4_quantize(_t(X, dev), _t(U.T, dev) if rank else None, BLOCK)
+    qw, sw, _ = qg.w4a4_quantize(_t(W, dev), None, BLOCK)
+    ta = _t(alpha, dev) if affine else None
+    kw = dict(XU=xu if rank else None, Vt=_t(V.T, dev) if rank else None, bias=_t(b, dev) if bias else None)
+    Y0 = qg.w4a4_gemm(qx, sx, qw, sw, K, alpha=ta, **kw).cpu().numpy()
+    packed = qg.w4a4_prepack_weights(qw, sw, K, alpha=ta)
+    Y1 = qg.w4a4_gemm_prepacked(qx, sx, packed, N, K, **kw).cpu().numpy()
+    Y2 = qg.w4a4_gemm_prepacked(qx, sx, packed, N, K, **kw).cpu().numpy()  # the buffer is reusable
+    assert np.array_equal(Y0.view(np.uint16), Y1.view(np.uint16))
+    assert np.array_equal(Y1.view(np.uint16), Y2.view(np.uint16))
+    qx_r, sx_r = oracle.w4a4_quantize(X, BLOCK)
+    qw_r, sw_r = oracle.w4a4_quantize(W, BLOCK)
+    ref = oracle.w4a4_gemm(qx_r, sx_r, qw_r, sw_r, BLOCK, K,
+                           XU=xu.cpu().numpy().astype(np.float64) if rank else None,
+                           V=V if rank else None, bias=b if bias else None, alpha=alpha)
+    assert_fp16_close(Y1, ref, f"w4a4 prepacked {M}x{N}x{K}")
+
+
 def test_end_to_end_full_size_sampled(dev, oracle):
     """The W4A4 workload (M=4096, N=K=8192, rank 32): GPU quantizer + GPU GEMM
     against the oracle's quantize -> X.U -> block-scaled GEMM on sampled rows."""
