@@ -211,11 +211,17 @@ int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, 
 
 // -------------------------------------------------------- operand converters
 //
-// Both converters expand 16 source bytes into 32 destination bytes (int8 ->
+// Both converters expand 8 source bytes into 16 destination bytes (int8 ->
 // fp16; two packed nibbles -> two e4m3 bytes), so one kernel shape serves
-// both: threads over the 16-byte chunks of a row, CTAs strided over rows,
-// blockIdx.z selecting the operand (A and B in one launch).  Both are
-// HBM-bound: 3 bytes of traffic per int8 value, 1.5 per int4 value.
+// both: a warp takes a 512-byte segment of a source row, lane l the 8-byte
+// pieces at 8 l and 256 + 8 l, and writes their 16-byte results at 16 l and
+// 512 + 16 l of the 1024-byte output segment, so every store instruction of
+// the warp fills 512 contiguous bytes (a thread converting 16 contiguous
+// source bytes would store two 16-byte halves 32 bytes apart, half-filling
+// the sectors of each store: 86 us against 70 us for two 8192 x 8192 int8
+// operands).  CTAs are strided over rows, blockIdx.z selects the operand (A
+// and B in one launch).  Both are HBM-bound: 3 bytes of traffic per int8
+// value, 1.5 per int4 value.
 
 struct ExpandJob {
     const uint8_t* src;
@@ -228,24 +234,21 @@ struct ExpandJobs {
     int64_t chunks;     // 16-byte source chunks per row (same for every job)
 };
 
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 
 // int8 -> fp16, exact: the byte XOR 0x80 (offset binary, 0..255) placed under
 // the fp16 exponent of 1024 is 1024 + b + 128; subtracting 1152 leaves b.
 struct S8ToF16 {
-    __device__ __forceinline__ void operator()(const uint4& in, uint4 (&out)[2]) const {
+    __device__ __forceinline__ uint4 operator()(const uint2& in) const {
         const __half2 c1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        const uint32_t w[4] = {in.x ^ 0x80808080u, in.y ^ 0x80808080u, in.z ^ 0x80808080u,
-                               in.w ^ 0x80808080u};
-        uint32_t o[8];
+        const uint32_t w[2] = {in.x ^ 0x80808080u, in.y ^ 0x80808080u};
+        uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const uint32_t lo = __byte_perm(w[q], 0x64646464u, 0x4140);  // bytes 0, 1
             const uint32_t hi = __byte_perm(w[q], 0x64646464u, 0x4342);  // bytes 2, 3
             __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), c1152);
@@ -253,8 +256,7 @@ struct S8ToF16 {
             o[2 * q] = *reinterpret_cast<uint32_t*>(&a);
             o[2 * q + 1] = *reinterpret_cast<uint32_t*>(&b);
         }
-        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        return make_uint4(o[0], o[1], o[2], o[3]);
     }
 };
 
@@ -297,9 +299,8 @@ struct S4ToE4M3 {
         const uint32_t sign = (mag + 0x7F7F7F7Fu) & 0x80808080u;
         return pos | mag | sign;
     }
-    __device__ __forceinline__ void operator()(const uint4& in, uint4 (&out)[2]) const {
-        out[0] = make_uint4(four(in.x & 0xFFFFu), four(in.x >> 16), four(in.y & 0xFFFFu), four(in.y >> 16));
-        out[1] = make_uint4(four(in.z & 0xFFFFu), four(in.z >> 16), four(in.w & 0xFFFFu), four(in.w >> 16));
+    __device__ __forceinline__ uint4 operator()(const uint2& in) const {
+        return make_uint4(four(in.x & 0xFFFFu), four(in.x >> 16), four(in.y & 0xFFFFu), four(in.y >> 16));
     }
 };
 
@@ -307,36 +308,45 @@ template <class Conv>
 __global__ void __launch_bounds__(256) k_expand(const ExpandJobs jobs) {
     const ExpandJob jb = blockIdx.z == 0 ? jobs.job[0] : jobs.job[1];  // no dynamic index into parameters
     const Conv conv;
-    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (c >= jobs.chunks) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t row_bytes = 16 * jobs.chunks;
+    const int64_t soff = (blockIdx.x * 8 + (threadIdx.x >> 5)) * 512 + 8 * lane;
+    if (soff >= row_bytes) return;
+    // the last segment of a row may be partial: each 8-byte piece is whole
+    // (row_bytes is a multiple of 16) and either inside the row or not
+    const bool second = soff + 256 < row_bytes;
+    const int64_t doff = 2 * soff;
     // four rows per pass, loads first: 64 bytes in flight per thread
     constexpr int U = 4;
     const int64_t step = gridDim.y;
     int64_t r = blockIdx.y;
     for (; r + (U - 1) * step < jb.rows; r += U * step) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = ld_stream16(jb.src + (r + u * step) * jb.lds + 16 * c);
+        uint2 v[U][2];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            uint4 o[2];
-            conv(v[u], o);
-            uint4* d = reinterpret_cast<uint4*>(jb.dst + (r + u * step) * jb.ldd + 32 * c);
-            d[0] = o[0];
-            d[1] = o[1];
+            const uint8_t* p = jb.src + (r + u * step) * jb.lds + soff;
+            v[u][0] = ld_stream8(p);
+            v[u][1] = second ? ld_stream8(p + 256) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint8_t* d = jb.dst + (r + u * step) * jb.ldd + doff;
+            *reinterpret_cast<uint4*>(d) = conv(v[u][0]);
+            if (second) *reinterpret_cast<uint4*>(d + 512) = conv(v[u][1]);
         }
     }
     for (; r < jb.rows; r += step) {
-        const uint4 v = ld_stream16(jb.src + r * jb.lds + 16 * c);
-        uint4 o[2];
-        conv(v, o);
-        uint4* d = reinterpret_cast<uint4*>(jb.dst + r * jb.ldd + 32 * c);
-        d[0] = o[0];
-        d[1] = o[1];
+        const uint8_t* p = jb.src + r * jb.lds + soff;
+        uint8_t* d = jb.dst + r * jb.ldd + doff;
+        *reinterpret_cast<uint4*>(d) = conv(ld_stream8(p));
+        if (second) *reinterpret_cast<uint4*>(d + 512) = conv(ld_stream8(p + 256));
     }
 }
 
-// Launches k_expand over one or two operands with the same chunk count.
+// Launches k_expand over one or two operands with the same chunk count: 8
+// warps (eight 512-byte source segments) per CTA along a row, up to 16 CTAs
+// per SM in all (two waves of 8; measured 3% faster than one wave at two
+// 8192 x 8192 int8 operands).
 template <class Conv>
 static int launch_expand(const ExpandJob* jobs, int njobs, int64_t chunks, int dev, cudaStream_t s) {
     ExpandJobs js;
@@ -345,8 +355,9 @@ static int launch_expand(const ExpandJob* jobs, int njobs, int64_t chunks, int d
     js.chunks = chunks;
     int64_t rows = jobs[0].rows;
     if (njobs > 1 && jobs[1].rows > rows) rows = jobs[1].rows;
-    const int64_t gx = (chunks + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms(dev)) * 8 / njobs;
+    const int64_t segs = (chunks + 31) / 32;  // 512-byte source segments per row
+    const int64_t gx = (segs + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(num_sms(dev)) * 16 / njobs;
     int64_t gy = cap / gx;
     if (gy > rows) gy = rows;
     if (gy > 65535) gy = 65535;
