@@ -122,6 +122,21 @@ __device__ __forceinline__ void st_global_16(void* dst, uint4 v, bool cs) {
         *reinterpret_cast<uint4*>(dst) = v;
 }
 
+// One 32-byte store (dst 32-byte aligned).  An epilogue thread owns one
+// output row, so the lanes of a warp store to 32 different rows: a 32-byte
+// piece per lane fills whole sectors, where 16-byte pieces would half-fill
+// each sector and take twice the store instructions.
+__device__ __forceinline__ void st_global_32(void* dst, uint4 a, uint4 b, bool cs) {
+    if (cs)
+        asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x),
+                     "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+    else
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x),
+                     "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                     : "memory");
+}
+
 // Tiles are visited in groups of `group_m` row-blocks (column-major inside a
 // group) so that the CTAs running at the same time cover a compact block of
 // the output and share their A and B tiles through L2: one CTA per SM covers
@@ -139,54 +154,73 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
     nb = local / gm;
 }
 
+__device__ __forceinline__ uint4 pack_f16x8(const float* f) {
+    uint4 pk;
+    __half2 h0 = __floats2half2_rn(f[0], f[1]);
+    __half2 h1 = __floats2half2_rn(f[2], f[3]);
+    __half2 h2 = __floats2half2_rn(f[4], f[5]);
+    __half2 h3 = __floats2half2_rn(f[6], f[7]);
+    pk.x = *reinterpret_cast<uint32_t*>(&h0);
+    pk.y = *reinterpret_cast<uint32_t*>(&h1);
+    pk.z = *reinterpret_cast<uint32_t*>(&h2);
+    pk.w = *reinterpret_cast<uint32_t*>(&h3);
+    return pk;
+}
+
 template <int N>
 __device__ __forceinline__ void store_row_f16(__half* dst, int col0, int N_total, const float* v,
                                               const __half* bias, bool cs = false) {
 #pragma unroll
-    for (int c = 0; c < N; c += 8) {
-        float f[8];
+    for (int c = 0; c < N; c += 16) {
+        float f[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = v[c + i];
+        for (int i = 0; i < 16; ++i) f[i] = v[c + i];
         if (bias) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 16; ++i) {
                 const int col = col0 + c + i;
                 if (col < N_total) f[i] += __half2float(bias[col]);
             }
         }
-        if (col0 + c + 8 <= N_total && (reinterpret_cast<uintptr_t>(dst + c) & 15u) == 0) {
-            uint4 pk;
-            __half2 h0 = __floats2half2_rn(f[0], f[1]);
-            __half2 h1 = __floats2half2_rn(f[2], f[3]);
-            __half2 h2 = __floats2half2_rn(f[4], f[5]);
-            __half2 h3 = __floats2half2_rn(f[6], f[7]);
-            pk.x = *reinterpret_cast<uint32_t*>(&h0);
-            pk.y = *reinterpret_cast<uint32_t*>(&h1);
-            pk.z = *reinterpret_cast<uint32_t*>(&h2);
-            pk.w = *reinterpret_cast<uint32_t*>(&h3);
-            st_global_16(dst + c, pk, cs);
-        } else {
+        if (col0 + c + 16 <= N_total && (reinterpret_cast<uintptr_t>(dst + c) & 31u) == 0) {
+            st_global_32(dst + c, pack_f16x8(f), pack_f16x8(f + 8), cs);
+            continue;
+        }
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (col0 + c + i < N_total) dst[c + i] = __float2half_rn(f[i]);
+        for (int h = 0; h < 16; h += 8) {
+            if (col0 + c + h + 8 <= N_total && (reinterpret_cast<uintptr_t>(dst + c + h) & 15u) == 0) {
+                st_global_16(dst + c + h, pack_f16x8(f + h), cs);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (col0 + c + h + i < N_total) dst[c + h + i] = __float2half_rn(f[h + i]);
+            }
         }
     }
 }
 
-template <int N>
+template <int N>  // N: a multiple of 8
 __device__ __forceinline__ void store_row_s32(int32_t* dst, int col0, int N_total,
                                               const int32_t* v, bool cs = false) {
+    auto pack4 = [&](int c) {
+        return make_uint4(static_cast<uint32_t>(v[c]), static_cast<uint32_t>(v[c + 1]),
+                          static_cast<uint32_t>(v[c + 2]), static_cast<uint32_t>(v[c + 3]));
+    };
 #pragma unroll
-    for (int c = 0; c < N; c += 4) {
-        if (col0 + c + 4 <= N_total && (reinterpret_cast<uintptr_t>(dst + c) & 15u) == 0) {
-            st_global_16(dst + c,
-                         make_uint4(static_cast<uint32_t>(v[c]), static_cast<uint32_t>(v[c + 1]),
-                                    static_cast<uint32_t>(v[c + 2]), static_cast<uint32_t>(v[c + 3])),
-                         cs);
-        } else {
+    for (int c = 0; c < N; c += 8) {
+        if (col0 + c + 8 <= N_total && (reinterpret_cast<uintptr_t>(dst + c) & 31u) == 0) {
+            st_global_32(dst + c, pack4(c), pack4(c + 4), cs);
+            continue;
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (col0 + c + i < N_total) dst[c + i] = v[c + i];
+        for (int h = 0; h < 8; h += 4) {
+            if (col0 + c + h + 4 <= N_total && (reinterpret_cast<uintptr_t>(dst + c + h) & 15u) == 0) {
+                st_global_16(dst + c + h, pack4(c + h), cs);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (col0 + c + h + i < N_total) dst[c + h + i] = v[c + h + i];
+            }
         }
     }
 }
