@@ -47,7 +47,7 @@ FP8_RATIO, FP4_RATIO = 2.0, 6.0
 # DRAM bytes (read + write) of one qgemm_s8 main-kernel launch at 8192^3, from
 # Nsight Compute (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # measured for the current kernel (the capture command is in the profiles).
-S8_MAIN_DRAM_BYTES = None
+S8_MAIN_DRAM_BYTES = 1104459776 + 253241856
 
 # Performance-regression floors: (breakdown entry, key) -> lowest accepted
 # fraction of its peak, about 15% under what GB300 measures.  The line
