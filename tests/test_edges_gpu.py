@@ -174,6 +174,54 @@ def test_gemm_f16_writes_only_its_output(dev, oracle, gemm_path, path):
     assert_fp16_close(C.cpu().numpy(), oracle.gemm_f16(A, B), "gemm_f16 guarded")
 
 
+def _guarded_16(M, N, dtype, dev):
+    """Like _guarded, but the row stride is 16 bytes past a multiple of 32:
+    the rows alternate between 32-byte aligned starts (32-byte stores) and
+    starts that are 16-byte aligned only (16-byte stores)."""
+    import torch
+    esz = 4 if dtype == torch.int32 else 2
+    ld = (N + 13 + 15) // 16 * 16 + 16 // esz
+    assert (ld * esz) % 32 == 16
+    if dtype == torch.int32:
+        buf = torch.full((M + 2, ld), SENTINEL_I32, dtype=torch.int32, device=dev)
+    else:
+        buf = torch.full((M + 2, ld), SENTINEL_F16, dtype=torch.int16, device=dev).view(torch.float16)
+    return buf, buf[1:M + 1, :N]
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_gemm_outputs_with_16_byte_row_alignment(dev, oracle, gemm_path, path):
+    import torch
+    import bit_quantized_tensor_gb300 as qg
+    gemm_path(path)
+    M, N, K = 300, 299, 160
+    A = inputs.s8_uniform(M, K, 1900)
+    B = inputs.s8_uniform(N, K, 2900)
+    buf, C = _guarded_16(M, N, torch.int32, dev)
+    qg.qgemm_s8(_t(A, dev), _t(B, dev), C=C)
+    torch.cuda.synchronize()
+    _check_guards(buf, M, N)
+    got, ref = C.cpu().numpy(), oracle.gemm_s8(A, B)
+    assert np.array_equal(got, ref), "s8: " + first_mismatch(got, ref)
+
+    A4 = inputs.s4_packed_uniform(M, K, 1901)
+    B4 = inputs.s4_packed_uniform(N, K, 2901)
+    buf, C = _guarded_16(M, N, torch.int32, dev)
+    qg.qgemm_s4(_t(A4, dev), _t(B4, dev), K, C=C)
+    torch.cuda.synchronize()
+    _check_guards(buf, M, N)
+    got, ref = C.cpu().numpy(), oracle.gemm_s4(A4, B4, K)
+    assert np.array_equal(got, ref), "s4: " + first_mismatch(got, ref)
+
+    Ah = inputs.f16_normal(M, K, 1902)
+    Bh = inputs.f16_normal(N, K, 2902)
+    buf, C = _guarded_16(M, N, torch.float16, dev)
+    qg.gemm_f16(_t(Ah, dev), _t(Bh, dev), C=C)
+    torch.cuda.synchronize()
+    _check_guards(buf, M, N)
+    assert_fp16_close(C.cpu().numpy(), oracle.gemm_f16(Ah, Bh), "gemm_f16 16-byte rows")
+
+
 # M = 1 and 5: GEMV with staged X; 12: GEMV with X from L2; 130: tensor-core
 # path with a ragged second launch of 2 rows
 @pytest.mark.parametrize("M,N,K", [(1, 4100, 512), (5, 300, 1024), (12, 2000, 768), (130, 260, 512)])
