@@ -63,9 +63,8 @@ __global__ void k_selftest_deadlock(Ctl ctl, int pattern) {
         if (warp == 2) bounded_wait(smem_u32(&bar[0]), 0u, abort_ptr, ctl, kSiteMissingArrival);
     } else if (pattern == kPhaseMismatch) {
         if (warp == 1) {
-            PipeState<1> st;
-            st.phase = 1u;  // wrong initial parity
-            bounded_wait(smem_u32(&bar[0]), st.phase, abort_ptr, ctl, kSitePhaseMismatch);
+            const uint32_t wrong_parity = 1u;  // a consumer that starts on the wrong phase
+            bounded_wait(smem_u32(&bar[0]), wrong_parity, abort_ptr, ctl, kSitePhaseMismatch);
         }
     } else {  // kCycle: bar[0] = full (MMA -> drain), bar[1] = empty (drain -> MMA)
         if (warp == 0) {  // drain

@@ -14,6 +14,7 @@
 //                constant-1 row for the low-rank unit).
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "qg_gemm_host.h"
@@ -22,6 +23,11 @@
 #include "w4a4_gemm2.cuh"
 
 namespace qg {
+
+// Which paired W4A4 kernel runs (qg_set_w4a4_pair_form): 0 the default
+// (256 x 256 tiles), 1 256 x 192 tiles.
+static std::atomic<int> g_w4a4_pair_form{0};
+static int w4a4_pair_form() { return g_w4a4_pair_form.load(); }
 
 constexpr int kW4A4Block = 64;
 constexpr int kW4A4MaxRank = 32;
@@ -355,7 +361,7 @@ namespace qg {
 
 // Tensor maps and launch of one of the two W4A4 GEMM kernels (one CTA per
 // 128 x 192 tile, or CTA pairs per 256 x 192 tile).
-template <class Cfg, bool PAIR>
+template <class Cfg, bool PAIR, auto KERNEL>
 static int launch_w4a4(const uint8_t* A8, const uint8_t* B8, const float* SXt, const float* SWt,
                        const uint16_t* XU, const uint16_t* V, int64_t M, int64_t N, int64_t K,
                        int64_t Mp, int64_t Np, int64_t rank, const W4A4Params& p, int dev,
@@ -379,7 +385,7 @@ static int launch_w4a4(const uint8_t* A8, const uint8_t* B8, const float* SXt, c
     }
     if (rc) return rc;
 
-    auto kernel = PAIR ? w4a4_gemm2_kernel : w4a4_gemm_kernel;
+    auto kernel = KERNEL;
     static std::mutex mu;
     static bool attr_set[64] = {};
     {
@@ -419,7 +425,11 @@ QG_KERNEL_BUDGET("k_w4a4_quantize<false>", reinterpret_cast<const void*>(k_w4a4_
 QG_KERNEL_BUDGET("k_scales_transposed", reinterpret_cast<const void*>(k_scales_transposed), 256, 0, 0, 1, 1);
 QG_KERNEL_BUDGET("w4a4_gemm_kernel", reinterpret_cast<const void*>(w4a4_gemm_kernel), W4A4Cfg::THREADS,
                  W4A4Cfg::SMEM_BYTES, W4A4Cfg::TMEM_COLS, 1, 1);
-QG_KERNEL_BUDGET("w4a4_gemm2_kernel", reinterpret_cast<const void*>(w4a4_gemm2_kernel), W4A4PairCfg::THREADS,
+QG_KERNEL_BUDGET("w4a4_gemm2_kernel<W4A4PairCfgT<256,4>>",
+                 reinterpret_cast<const void*>(w4a4_gemm2_kernel<W4A4PairCfgT<256, 4>>),
+                 W4A4PairCfgT<256, 4>::THREADS, W4A4PairCfgT<256, 4>::SMEM_BYTES, W4A4PairCfgT<256, 4>::TMEM_COLS,
+                 2, 1);
+QG_KERNEL_BUDGET("w4a4_gemm2_kernel", reinterpret_cast<const void*>(w4a4_gemm2_kernel<W4A4PairCfg>), W4A4PairCfg::THREADS,
                  W4A4PairCfg::SMEM_BYTES, W4A4PairCfg::TMEM_COLS, 2, 1);
 
 }  // namespace qg
@@ -501,8 +511,17 @@ static int w4a4_run(int64_t M, int64_t N, int64_t K, const uint8_t* A8, const fl
     p.ctl = ctl;
     const int path = gemm_path();
     const bool pairs = path == 2 || (path == 0 && M > W4A4Cfg::BM);
-    return pairs ? launch_w4a4<W4A4PairCfg, true>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s)
-                 : launch_w4a4<W4A4Cfg, false>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p, dev, s);
+    if (!pairs)
+        return launch_w4a4<W4A4Cfg, false, w4a4_gemm_kernel>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank,
+                                                             p, dev, s);
+    // 256 x 256 tiles (four epilogue warps per TMEM lane quadrant) by
+    // default; 256 x 192 tiles (three per quadrant) as the ablation form
+    using P256 = W4A4PairCfgT<256, 4>;
+    if (w4a4_pair_form() == 1)
+        return launch_w4a4<W4A4PairCfg, true, w4a4_gemm2_kernel<W4A4PairCfg>>(A8, B8, SXt, SWt, XU, V, M, N, K,
+                                                                               Mp, Np, rank, p, dev, s);
+    return launch_w4a4<P256, true, w4a4_gemm2_kernel<P256>>(A8, B8, SXt, SWt, XU, V, M, N, K, Mp, Np, rank, p,
+                                                             dev, s);
 }
 
 // w4a4_gemm and w4a4_gemm_affine: alpha == nullptr is the formula as printed.
@@ -638,6 +657,12 @@ int w4a4_gemm_prepacked(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, cons
     const uint8_t* B8 = static_cast<const uint8_t*>(packed);
     const float* SWt = reinterpret_cast<const float*>(B8 + w4a4_packed_scales_offset(N, K));
     return w4a4_run(M, N, K, A8, SXt, B8, SWt, XU, V, rank, bias, Y, ldy, ctl, dev, s);
+}
+
+int qg_set_w4a4_pair_form(int form) {
+    if (form < 0 || form > 1) return QG_ERR_INVALID_ARG;
+    g_w4a4_pair_form.store(form);
+    return QG_OK;
 }
 
 }  // extern "C"

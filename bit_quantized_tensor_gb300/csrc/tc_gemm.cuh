@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            PipeState<STAGES> ps;
+            Ring<STAGES> ps;
             uint32_t armed = 0, armed_phase = 0;  // bit s: slot s armed / its phase
             const L2Policies pol = l2_policies(p.l2_mode);
             bool ok = true;
@@ -286,19 +286,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int mb, nb;
                 tile_coords(t, num_m, num_n, mb, nb);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!bounded_wait(empty_bar(ps.index), ps.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(ps.index), Cfg::STAGE_BYTES);
-                    tma_load_2d(smem_u32(sA + ps.index * Cfg::A_BYTES), &tmA, kb * Cfg::BK,
-                                mb * Cfg::BM, full_bar(ps.index), pol.a);
-                    tma_load_2d(smem_u32(sB + ps.index * Cfg::B_BYTES), &tmB, kb * Cfg::BK,
-                                nb * Cfg::BN, full_bar(ps.index), pol.b);
-                    armed |= 1u << ps.index;
-                    armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
-                    ps.advance();
+                    mbar_arrive_expect_tx(full_bar(ps.slot()), Cfg::STAGE_BYTES);
+                    tma_load_2d(smem_u32(sA + ps.slot() * Cfg::A_BYTES), &tmA, kb * Cfg::BK,
+                                mb * Cfg::BM, full_bar(ps.slot()), pol.a);
+                    tma_load_2d(smem_u32(sB + ps.slot() * Cfg::B_BYTES), &tmB, kb * Cfg::BK,
+                                nb * Cfg::BN, full_bar(ps.slot()), pol.b);
+                    armed |= 1u << ps.slot();
+                    armed_phase = (armed_phase & ~(1u << ps.slot())) | (ps.parity() << ps.slot());
+                    ps.next();
                 }
             }
             if (!ok) {
@@ -312,29 +312,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            PipeState<STAGES> ps;
-            PipeState<ACC_BUFS> as;
+            Ring<STAGES> ps;
+            Ring<ACC_BUFS> as;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
                 for (int u = 0; ok && u < units; ++u) {
                     const int kb0 = u * p.chunk_kb;
                     const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
-                    if (!bounded_wait(acce_bar(as.index), as.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(acce_bar(as.slot()), as.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteMmaAccEmpty)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as.index * Cfg::BN);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as.slot() * Cfg::BN);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!bounded_wait(full_bar(ps.index), ps.phase, abort_flag, p.ctl,
+                        if (!bounded_wait(full_bar(ps.slot()), ps.parity(), abort_flag, p.ctl,
                                           kSiteMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                        const uint32_t a_addr = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
 #pragma unroll
                         for (int k = 0; k < Cfg::KSTEPS; ++k) {
                             const uint64_t ad = smem_desc_sw128(a_addr + 32u * k);
@@ -342,12 +342,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             tc_mma<Cfg::KIND>(d_tmem, ad, bd, Cfg::IDESC,
                                               (kb > kb0 || k > 0) ? 1u : 0u);
                         }
-                        tc_commit(empty_bar(ps.index));
-                        ps.advance();
+                        tc_commit(empty_bar(ps.slot()));
+                        ps.next();
                     }
                     if (!ok) break;
-                    tc_commit(accf_bar(as.index));
-                    as.advance();
+                    tc_commit(accf_bar(as.slot()));
+                    as.next();
                 }
             }
             // Every MMA issued by this thread has completed before the CTA
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ---------------------------------------------------- epilogue
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
         const int colhalf = (warp - 2) >> 2;     // 0: columns [0,128), 1: [128,256)
-        PipeState<ACC_BUFS> as;
+        Ring<ACC_BUFS> as;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
             int mb, nb;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 128; ++i) sum[i] = 0;
                 for (int u = 0; u < units; ++u) {
-                    bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                    bool got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                             kSiteEpiAccFull);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(as.index * Cfg::BN + colhalf * 128);
+                                           static_cast<uint32_t>(as.slot() * Cfg::BN + colhalf * 128);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
@@ -391,8 +391,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(as.index));
-                    as.advance();
+                    if (lane == 0) mbar_arrive(acce_bar(as.slot()));
+                    as.next();
                 }
                 if (!ok) break;
                 if (row < p.M)
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                            col0,
                                        col0, p.N, sum, p.l2_mode == 2);
             } else {
-                bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                bool got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                         kSiteEpiAccFull);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(as.index * Cfg::BN + colhalf * 128);
+                                       static_cast<uint32_t>(as.slot() * Cfg::BN + colhalf * 128);
                 float v[128];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -420,8 +420,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce_bar(as.index));
-                as.advance();
+                if (lane == 0) mbar_arrive(acce_bar(as.slot()));
+                as.next();
                 if (row < p.M)
                     store_row_f16<128>(static_cast<__half*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,

@@ -11,7 +11,7 @@
 // "Warp-Specialized Kernel Implementation for W4A4 MatMul on Latest GPU
 // Architectures", section 4, with the data flow re-divided as it describes.
 //
-// Synchronization (each role keeps its own PipeState):
+// Synchronization (each role keeps its own position in each ring it walks):
 //   full[s]      leader only; armed by the leader's producer for both CTAs'
 //                bytes, completed by both CTAs' TMA loads (cta_group::2 TMA
 //                signals the leader's barrier)
@@ -127,7 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
-            PipeState<STAGES> ps;
+            Ring<STAGES> ps;
             uint32_t armed = 0, armed_phase = 0;
             const L2Policies pol = l2_policies(p.l2_mode);
             bool ok = true;
@@ -137,22 +137,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 const int arow = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM;
                 const int brow = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!bounded_wait(empty_bar(ps.index), ps.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
                                       kSitePairProdEmpty)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t lead_full = mapa_shared(full_bar(ps.index), 0);
+                    const uint32_t lead_full = mapa_shared(full_bar(ps.slot()), 0);
                     if (leader) {
-                        mbar_arrive_expect_tx(full_bar(ps.index), 2 * Cfg::STAGE_BYTES);
-                        armed |= 1u << ps.index;
-                        armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
+                        mbar_arrive_expect_tx(full_bar(ps.slot()), 2 * Cfg::STAGE_BYTES);
+                        armed |= 1u << ps.slot();
+                        armed_phase = (armed_phase & ~(1u << ps.slot())) | (ps.parity() << ps.slot());
                     }
-                    tma_load_2d_pair(smem_u32(sA + ps.index * Cfg::A_BYTES), &tmA, kb * Cfg::BK, arow,
+                    tma_load_2d_pair(smem_u32(sA + ps.slot() * Cfg::A_BYTES), &tmA, kb * Cfg::BK, arow,
                                      lead_full, pol.a);
-                    tma_load_2d_pair(smem_u32(sB + ps.index * Cfg::B_BYTES), &tmB, kb * Cfg::BK, brow,
+                    tma_load_2d_pair(smem_u32(sB + ps.slot() * Cfg::B_BYTES), &tmB, kb * Cfg::BK, brow,
                                      lead_full, pol.b);
-                    ps.advance();
+                    ps.next();
                 }
             }
             if (!ok) {
@@ -174,40 +174,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (leader)
-            PipeState<STAGES> ps;
-            PipeState<ACC_BUFS> as;
+            Ring<STAGES> ps;
+            Ring<ACC_BUFS> as;
             bool ok = true;
             for (int t = pair; ok && t < ntiles; t += npairs) {
                 for (int u = 0; ok && u < units; ++u) {
                     const int kb0 = u * p.chunk_kb;
                     const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
-                    if (!bounded_wait(acce_bar(as.index), as.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(acce_bar(as.slot()), as.parity() ^ 1u, abort_flag, p.ctl,
                                       kSitePairMmaAcc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as.index * Cfg::BN);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as.slot() * Cfg::BN);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!bounded_wait(full_bar(ps.index), ps.phase, abort_flag, p.ctl,
+                        if (!bounded_wait(full_bar(ps.slot()), ps.parity(), abort_flag, p.ctl,
                                           kSitePairMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                        const uint32_t a_addr = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
 #pragma unroll
                         for (int k = 0; k < Cfg::KSTEPS; ++k)
                             tc_mma_pair<Cfg::KIND>(d_tmem, smem_desc_sw128(a_addr + 32u * k),
                                                    smem_desc_sw128(b_addr + 32u * k), Cfg::IDESC,
                                                    (kb > kb0 || k > 0) ? 1u : 0u);
-                        tc_commit_pair(empty_bar(ps.index), 0x3);
-                        ps.advance();
+                        tc_commit_pair(empty_bar(ps.slot()), 0x3);
+                        ps.next();
                     }
                     if (!ok) break;
-                    tc_commit_pair(accf_bar(as.index), 0x3);
-                    as.advance();
+                    tc_commit_pair(accf_bar(as.slot()), 0x3);
+                    as.next();
                 }
             }
             tc_commit_pair(drain_bar, 0x1);
@@ -217,7 +217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         // ---------------------------------------------------- epilogue (both CTAs)
         const int quad = warp & 3;
         const int colhalf = (warp - 2) >> 2;
-        PipeState<ACC_BUFS> as;
+        Ring<ACC_BUFS> as;
         bool ok = true;
         for (int t = pair; ok && t < ntiles; t += npairs) {
             int mb, nb;
@@ -229,7 +229,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 128; ++i) sum[i] = 0;
                 for (int u = 0; u < units; ++u) {
-                    bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                    bool got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                             kSitePairEpiAcc);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
@@ -237,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(as.index * Cfg::BN + colhalf * 128);
+                                           static_cast<uint32_t>(as.slot() * Cfg::BN + colhalf * 128);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
@@ -251,8 +251,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     // leader needs the arrival only, not a cluster-scope release.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.index), 0));
-                    as.advance();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.slot()), 0));
+                    as.next();
                 }
                 if (!ok) break;
                 if (row < p.M)
@@ -260,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                                            col0,
                                        col0, p.N, sum, p.l2_mode == 2);
             } else {
-                bool got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                bool got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                         kSitePairEpiAcc);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
@@ -268,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(as.index * Cfg::BN + colhalf * 128);
+                                       static_cast<uint32_t>(as.slot() * Cfg::BN + colhalf * 128);
                 float v[128];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -280,8 +280,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.index), 0));
-                as.advance();
+                if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce_bar(as.slot()), 0));
+                as.next();
                 if (row < p.M)
                     store_row_f16<128>(static_cast<__half*>(p.C) + static_cast<int64_t>(row) * p.ldc +
                                            col0,

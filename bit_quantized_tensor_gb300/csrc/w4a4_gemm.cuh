@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            PipeState<STAGES> ps;
-            PipeState<SCS> ss;
+            Ring<STAGES> ps;
+            Ring<SCS> ss;
             uint32_t armed = 0, armed_phase = 0, sarmed = 0, sarmed_phase = 0;
             const uint64_t pol = l2_policy_evict_normal();
             bool ok = true;
@@ -186,38 +186,38 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                 const int steps = p.num_ks + p.lowrank;
                 for (int ks = 0; ks < steps; ++ks) {
                     const bool lr = ks == p.num_ks;
-                    if (!bounded_wait(empty_bar(ps.index), ps.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteW4ProdEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(ps.index), Cfg::STAGE_BYTES);
-                    const uint32_t da = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                    const uint32_t db = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                    mbar_arrive_expect_tx(full_bar(ps.slot()), Cfg::STAGE_BYTES);
+                    const uint32_t da = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                    const uint32_t db = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
                     if (!lr) {
-                        tma_load_2d(da, &tmA, ks * Cfg::BK, mb * Cfg::BM, full_bar(ps.index), pol);
-                        tma_load_2d(db, &tmB, ks * Cfg::BK, nb * Cfg::BN, full_bar(ps.index), pol);
+                        tma_load_2d(da, &tmA, ks * Cfg::BK, mb * Cfg::BM, full_bar(ps.slot()), pol);
+                        tma_load_2d(db, &tmB, ks * Cfg::BK, nb * Cfg::BN, full_bar(ps.slot()), pol);
                     } else {
-                        tma_load_2d(da, &tmXU, 0, mb * Cfg::BM, full_bar(ps.index), pol);
-                        tma_load_2d(db, &tmV, 0, nb * Cfg::BN, full_bar(ps.index), pol);
+                        tma_load_2d(da, &tmXU, 0, mb * Cfg::BM, full_bar(ps.slot()), pol);
+                        tma_load_2d(db, &tmV, 0, nb * Cfg::BN, full_bar(ps.slot()), pol);
                     }
-                    armed |= 1u << ps.index;
-                    armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
-                    ps.advance();
+                    armed |= 1u << ps.slot();
+                    armed_phase = (armed_phase & ~(1u << ps.slot())) | (ps.parity() << ps.slot());
+                    ps.next();
 
-                    if (!bounded_wait(sce_bar(ss.index), ss.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(sce_bar(ss.slot()), ss.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteW4ProdScale)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(scf_bar(ss.index), Cfg::SC_BYTES);
-                    const uint32_t dsx = smem_u32(sS + ss.index * Cfg::SC_BYTES);
+                    mbar_arrive_expect_tx(scf_bar(ss.slot()), Cfg::SC_BYTES);
+                    const uint32_t dsx = smem_u32(sS + ss.slot() * Cfg::SC_BYTES);
                     const int row = lr ? p.nblk : 2 * ks;
-                    tma_load_2d(dsx, &tmSX, mb * Cfg::BM, row, scf_bar(ss.index), pol);
-                    tma_load_2d(dsx + Cfg::SX_BYTES, &tmSW, nb * Cfg::BN, row, scf_bar(ss.index), pol);
-                    sarmed |= 1u << ss.index;
-                    sarmed_phase = (sarmed_phase & ~(1u << ss.index)) | (ss.phase << ss.index);
-                    ss.advance();
+                    tma_load_2d(dsx, &tmSX, mb * Cfg::BM, row, scf_bar(ss.slot()), pol);
+                    tma_load_2d(dsx + Cfg::SX_BYTES, &tmSW, nb * Cfg::BN, row, scf_bar(ss.slot()), pol);
+                    sarmed |= 1u << ss.slot();
+                    sarmed_phase = (sarmed_phase & ~(1u << ss.slot())) | (ss.parity() << ss.slot());
+                    ss.next();
                 }
             }
             if (!ok) {
@@ -234,30 +234,30 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            PipeState<STAGES> ps;
-            PipeState<ACC> as;
+            Ring<STAGES> ps;
+            Ring<ACC> as;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
                 const int steps = p.num_ks + p.lowrank;
                 for (int ks = 0; ok && ks < steps; ++ks) {
                     const bool lr = ks == p.num_ks;
-                    if (!bounded_wait(full_bar(ps.index), ps.phase, abort_flag, p.ctl,
+                    if (!bounded_wait(full_bar(ps.slot()), ps.parity(), abort_flag, p.ctl,
                                       kSiteW4MmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                    const uint32_t a_addr = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
                     const int units = lr ? 1 : 2;
                     for (int h = 0; h < units; ++h) {
-                        if (!bounded_wait(acce_bar(as.index), as.phase ^ 1u, abort_flag, p.ctl,
+                        if (!bounded_wait(acce_bar(as.slot()), as.parity() ^ 1u, abort_flag, p.ctl,
                                           kSiteW4MmaAcc)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(as.index * Cfg::BN);
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(as.slot() * Cfg::BN);
                         if (!lr) {
                             // one 64-wide block = bytes [64h, 64h + 64) of each row: 2 MMAs
 #pragma unroll
@@ -274,12 +274,12 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                                                      smem_desc_sw128(b_addr + 32u * k), Cfg::IDESC,
                                                      k > 0 ? 1u : 0u);
                         }
-                        tc_commit(accf_bar(as.index));
-                        as.advance();
+                        tc_commit(accf_bar(as.slot()));
+                        as.next();
                     }
                     if (!ok) break;
-                    tc_commit(empty_bar(ps.index));
-                    ps.advance();
+                    tc_commit(empty_bar(ps.slot()));
+                    ps.next();
                 }
             }
             tc_commit(drain_bar);
@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
         const int colpart = (warp - 2) >> 2;     // which quarter of the tile's columns
         const int g = lane >> 2, q = lane & 3;
-        PipeState<ACC> as;
-        PipeState<SCS> ss;
+        Ring<ACC> as;
+        Ring<SCS> ss;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
             int mb, nb;
@@ -315,16 +315,16 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
             const int steps = p.num_ks + p.lowrank;
             for (int ks = 0; ok && ks < steps; ++ks) {
                 const int units = (ks == p.num_ks) ? 1 : 2;
-                bool got = bounded_wait(scf_bar(ss.index), ss.phase, abort_flag, p.ctl,
+                bool got = bounded_wait(scf_bar(ss.slot()), ss.parity(), abort_flag, p.ctl,
                                         kSiteW4EpiScale);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
-                const float* sx_s = reinterpret_cast<const float*>(sS + ss.index * Cfg::SC_BYTES);
+                const float* sx_s = reinterpret_cast<const float*>(sS + ss.slot() * Cfg::SC_BYTES);
                 const float* sw_s = sx_s + 2 * Cfg::BM;
                 for (int h = 0; h < units; ++h) {
-                    got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                    got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                        kSiteW4EpiAcc);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                     const float* sxr = sx_s + h * Cfg::BM + quad * 32 + g;
                     const float* swc = sw_s + h * Cfg::BN + colpart * Cfg::EPI_COLS + 2 * q;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(as.index * Cfg::BN +
+                                           static_cast<uint32_t>(as.slot() * Cfg::BN +
                                                                  colpart * Cfg::EPI_COLS);
                     uint32_t rb[2][2][8];  // [buffer][half][x2 registers]
 #pragma unroll
@@ -374,13 +374,13 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(as.index));
-                    as.advance();
+                    if (lane == 0) mbar_arrive(acce_bar(as.slot()));
+                    as.next();
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sce_bar(ss.index));
-                ss.advance();
+                if (lane == 0) mbar_arrive(sce_bar(ss.slot()));
+                ss.next();
             }
             if (!ok) break;
             // fp16 store (+ bias): per row pairs of adjacent columns

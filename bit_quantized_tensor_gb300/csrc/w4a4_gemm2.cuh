@@ -9,14 +9,15 @@
 // Kernel Implementation for W4A4 MatMul on Latest GPU Architectures",
 // sections 4 and 5.)
 //
-// What changes is the data flow.  The two CTAs of a cluster share a 256 x 192
-// output tile: CTA r owns rows [128 r, 128 r + 128), loads its own 128 rows of
-// A and its own 96 rows of B (half of the tile's columns), and the leader
-// issues tcgen05.mma.cta_group::2 with M = 256 that writes each CTA's
-// 128 x 192 block partial into that CTA's TMEM (two buffers).  Per 64-wide K
-// block an SM then loads 14 KB of operands for 128 x 192 outputs instead of
-// 20 KB in the one-CTA kernel, whose operand stream alone runs at the
-// L2-to-SM bandwidth.
+// What changes is the data flow.  The two CTAs of a cluster share a 256 x BN
+// output tile (BN = 256 by default, 192 as the ablation form): CTA r owns
+// rows [128 r, 128 r + 128), loads its own 128 rows of A and its own BN / 2
+// rows of B (half of the tile's columns), and the leader issues
+// tcgen05.mma.cta_group::2 with M = 256 that writes each CTA's 128 x BN
+// block partial into that CTA's TMEM (two buffers).  Per 64-wide K block an
+// SM then loads 8 KB of A and BN / 2 x 64 bytes of B; at BN = 256 each
+// paired fp8 MMA instruction (N = 256, K = 32) carries enough tensor work
+// to cover its own issue cost, which the N = 128 instruction does not.
 //
 // Synchronization:
 //   full[s]     leader only; armed by the leader's producer for both CTAs'
@@ -24,7 +25,7 @@
 //   empty[s]    both CTAs; one multicast commit from the leader
 //   scf/sce[s]  per CTA: its own scale tables (sX of its rows, sW of the tile)
 //   accf[b]     both CTAs; multicast commit after a block's MMAs
-//   acce[b]     leader only; the 16 epilogue warps of each CTA arrive remotely
+//   acce[b]     leader only; the epilogue warps of both CTAs arrive remotely
 //               (relaxed: one arrive per warp per 64-wide block)
 // Every wait is bounded; the CTAs leave only after a cluster barrier.
 #pragma once
@@ -32,9 +33,10 @@
 
 namespace qg {
 
-struct W4A4PairCfg {
+template <int BN_ = 192, int EPQ_ = 3>
+struct W4A4PairCfgT {
     static constexpr int BM = 128;                        // rows per CTA (256 per pair)
-    static constexpr int BN = 192;                        // columns of the pair's tile
+    static constexpr int BN = BN_;                        // columns of the pair's tile
     static constexpr int B_ROWS = BN / 2;                 // B rows loaded per CTA
     static constexpr int ROW_BYTES = 128;                 // 128 e4m3 per stage row = 2 blocks
     static constexpr int BK = 128;
@@ -54,8 +56,8 @@ struct W4A4PairCfg {
         STAGES * STAGE_BYTES + SC_STAGES * SC_BYTES + BARRIER_BYTES + ALIGN_SLACK;
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EPI_WARPS = 12;                  // 3 per TMEM lane quadrant
-    static constexpr int EPI_COLS = BN / 3;               // 64 columns per epilogue warp
+    static constexpr int EPI_WARPS = 4 * EPQ_;            // EPQ_ per TMEM lane quadrant
+    static constexpr int EPI_COLS = BN / EPQ_;            // columns per epilogue warp
     static constexpr int THREADS = 32 * (2 + EPI_WARPS);
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * SC_STAGES + 2 * ACC_BUFS + 1;
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, 2 * BM, BN);  // M = 256 across the pair
@@ -68,8 +70,9 @@ struct W4A4PairCfg {
     static_assert(SC_BYTES % 128 == 0 && B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0,
                   "alignment of ring slots");
     static_assert(EPI_COLS % 8 == 0, "epilogue reads 8-column groups");
-    static_assert(THREADS <= 512, "more than 4 warps per SM sub-partition cap registers at 96");
+    static_assert(THREADS <= 640, "register file split");
 };
+using W4A4PairCfg = W4A4PairCfgT<>;
 
 enum W4A4PairSite : int {
     kSiteW4PProdEmpty = 221,
@@ -82,12 +85,12 @@ enum W4A4PairSite : int {
     kSiteW4PDrainMma = 228,
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS, 1)
+template <class Cfg>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     w4a4_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmXU, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmSX, const __grid_constant__ CUtensorMap tmSW,
                       const W4A4Params p) {
-    using Cfg = W4A4PairCfg;
     constexpr int STAGES = Cfg::STAGES, SCS = Cfg::SC_STAGES, ACC = Cfg::ACC_BUFS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -149,8 +152,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
-            PipeState<STAGES> ps;
-            PipeState<SCS> ss;
+            Ring<STAGES> ps;
+            Ring<SCS> ss;
             uint32_t armed = 0, armed_phase = 0, sarmed = 0, sarmed_phase = 0;
             const uint64_t pol = l2_policy_evict_normal();
             bool ok = true;
@@ -161,19 +164,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                 const int brow = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 for (int ks = 0; ks < steps; ++ks) {
                     const bool lr = ks == p.num_ks;
-                    if (!bounded_wait(empty_bar(ps.index), ps.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteW4PProdEmpty)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t lead_full = mapa_shared(full_bar(ps.index), 0);
+                    const uint32_t lead_full = mapa_shared(full_bar(ps.slot()), 0);
                     if (leader) {
-                        mbar_arrive_expect_tx(full_bar(ps.index), 2 * Cfg::STAGE_BYTES);
-                        armed |= 1u << ps.index;
-                        armed_phase = (armed_phase & ~(1u << ps.index)) | (ps.phase << ps.index);
+                        mbar_arrive_expect_tx(full_bar(ps.slot()), 2 * Cfg::STAGE_BYTES);
+                        armed |= 1u << ps.slot();
+                        armed_phase = (armed_phase & ~(1u << ps.slot())) | (ps.parity() << ps.slot());
                     }
-                    const uint32_t da = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                    const uint32_t db = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                    const uint32_t da = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                    const uint32_t db = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
                     if (!lr) {
                         tma_load_2d_pair(da, &tmA, ks * Cfg::BK, arow, lead_full, pol);
                         tma_load_2d_pair(db, &tmB, ks * Cfg::BK, brow, lead_full, pol);
@@ -181,21 +184,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                         tma_load_2d_pair(da, &tmXU, 0, arow, lead_full, pol);
                         tma_load_2d_pair(db, &tmV, 0, brow, lead_full, pol);
                     }
-                    ps.advance();
+                    ps.next();
 
-                    if (!bounded_wait(sce_bar(ss.index), ss.phase ^ 1u, abort_flag, p.ctl,
+                    if (!bounded_wait(sce_bar(ss.slot()), ss.parity() ^ 1u, abort_flag, p.ctl,
                                       kSiteW4PProdScale)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(scf_bar(ss.index), Cfg::SC_BYTES);
-                    const uint32_t dsx = smem_u32(sS + ss.index * Cfg::SC_BYTES);
+                    mbar_arrive_expect_tx(scf_bar(ss.slot()), Cfg::SC_BYTES);
+                    const uint32_t dsx = smem_u32(sS + ss.slot() * Cfg::SC_BYTES);
                     const int row = lr ? p.nblk : 2 * ks;
-                    tma_load_2d(dsx, &tmSX, arow, row, scf_bar(ss.index), pol);
-                    tma_load_2d(dsx + Cfg::SX_BYTES, &tmSW, nb * Cfg::BN, row, scf_bar(ss.index), pol);
-                    sarmed |= 1u << ss.index;
-                    sarmed_phase = (sarmed_phase & ~(1u << ss.index)) | (ss.phase << ss.index);
-                    ss.advance();
+                    tma_load_2d(dsx, &tmSX, arow, row, scf_bar(ss.slot()), pol);
+                    tma_load_2d(dsx + Cfg::SX_BYTES, &tmSW, nb * Cfg::BN, row, scf_bar(ss.slot()), pol);
+                    sarmed |= 1u << ss.slot();
+                    sarmed_phase = (sarmed_phase & ~(1u << ss.slot())) | (ss.parity() << ss.slot());
+                    ss.next();
                 }
             }
             if (!ok) {
@@ -220,29 +223,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (leader)
-            PipeState<STAGES> ps;
-            PipeState<ACC> as;
+            Ring<STAGES> ps;
+            Ring<ACC> as;
             bool ok = true;
             for (int t = pair; ok && t < ntiles; t += npairs) {
                 for (int ks = 0; ok && ks < steps; ++ks) {
                     const bool lr = ks == p.num_ks;
-                    if (!bounded_wait(full_bar(ps.index), ps.phase, abort_flag, p.ctl,
+                    if (!bounded_wait(full_bar(ps.slot()), ps.parity(), abort_flag, p.ctl,
                                       kSiteW4PMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + ps.index * Cfg::A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + ps.index * Cfg::B_BYTES);
+                    const uint32_t a_addr = smem_u32(sA + ps.slot() * Cfg::A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + ps.slot() * Cfg::B_BYTES);
                     const int units = lr ? 1 : 2;
                     for (int h = 0; h < units; ++h) {
-                        if (!bounded_wait(acce_bar(as.index), as.phase ^ 1u, abort_flag, p.ctl,
+                        if (!bounded_wait(acce_bar(as.slot()), as.parity() ^ 1u, abort_flag, p.ctl,
                                           kSiteW4PMmaAcc)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(as.index * Cfg::BN);
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(as.slot() * Cfg::BN);
                         if (!lr) {
                             // one 64-wide block = bytes [64h, 64h + 64) of each row: 2 MMAs
 #pragma unroll
@@ -259,12 +262,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                                                           smem_desc_sw128(b_addr + 32u * k),
                                                           Cfg::IDESC, k > 0 ? 1u : 0u);
                         }
-                        tc_commit_pair(accf_bar(as.index), 0x3);
-                        as.advance();
+                        tc_commit_pair(accf_bar(as.slot()), 0x3);
+                        as.next();
                     }
                     if (!ok) break;
-                    tc_commit_pair(empty_bar(ps.index), 0x3);
-                    ps.advance();
+                    tc_commit_pair(empty_bar(ps.slot()), 0x3);
+                    ps.next();
                 }
             }
             tc_commit_pair(drain_bar, 0x1);
@@ -284,8 +287,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
         const int colpart = (warp - 2) >> 2;
         const int g = lane >> 2, q = lane & 3;
         const uint32_t lead_acce0 = mapa_shared(acce_bar(0), 0);
-        PipeState<ACC> as;
-        PipeState<SCS> ss;
+        Ring<ACC> as;
+        Ring<SCS> ss;
         bool ok = true;
         for (int t = pair; ok && t < ntiles; t += npairs) {
             int mb, nb;
@@ -300,16 +303,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                     for (int i = 0; i < 4; ++i) acc[hf][c][i] = 0.f;
             for (int ks = 0; ok && ks < steps; ++ks) {
                 const int units = (ks == p.num_ks) ? 1 : 2;
-                bool got = bounded_wait(scf_bar(ss.index), ss.phase, abort_flag, p.ctl,
+                bool got = bounded_wait(scf_bar(ss.slot()), ss.parity(), abort_flag, p.ctl,
                                         kSiteW4PEpiScale);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
-                const float* sx_s = reinterpret_cast<const float*>(sS + ss.index * Cfg::SC_BYTES);
+                const float* sx_s = reinterpret_cast<const float*>(sS + ss.slot() * Cfg::SC_BYTES);
                 const float* sw_s = sx_s + 2 * Cfg::BM;
                 for (int h = 0; h < units; ++h) {
-                    got = bounded_wait(accf_bar(as.index), as.phase, abort_flag, p.ctl,
+                    got = bounded_wait(accf_bar(as.slot()), as.parity(), abort_flag, p.ctl,
                                        kSiteW4PEpiAcc);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
@@ -317,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                     }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                           static_cast<uint32_t>(as.index * Cfg::BN +
+                                           static_cast<uint32_t>(as.slot() * Cfg::BN +
                                                                  colpart * Cfg::EPI_COLS);
                     const float* sxr = sx_s + h * Cfg::BM + quad * 32 + g;
                     const float* swc = sw_s + h * Cfg::BN + colpart * Cfg::EPI_COLS + 2 * q;
@@ -356,13 +359,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4A4PairCfg::THREADS
                     // leader needs the arrival only, not a cluster-scope release.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(lead_acce0 + 8u * as.index);
-                    as.advance();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(lead_acce0 + 8u * as.slot());
+                    as.next();
                 }
                 if (!ok) break;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sce_bar(ss.index));
-                ss.advance();
+                if (lane == 0) mbar_arrive(sce_bar(ss.slot()));
+                ss.next();
             }
             if (!ok) break;
             // fp16 store (+ bias): per row pairs of adjacent columns

@@ -162,6 +162,13 @@ int qg_set_s8_chunk(int kblocks);
  * 2 = always CTA pairs.  Results are identical; only speed differs. */
 int qg_set_gemm_path(int path);
 
+/* Ablation knob: tile of the paired kernel behind w4a4_gemm,
+ * w4a4_gemm_affine and w4a4_gemm_prepacked when M > 128.  0 = 256 x 256
+ * tiles with 16 epilogue warps (default), 1 = 256 x 192 tiles with 12.  The
+ * arithmetic and its order are the same, so the results are bit-identical;
+ * QG_ERR_INVALID_ARG for another value. */
+int qg_set_w4a4_pair_form(int form);
+
 /* L2 cache policy of the tensor-core GEMMs behind gemm_f16, qgemm_s8 and
  * qgemm_s4 (an ablation knob; results are identical in every mode):
  *   0 = every TMA operand load evict-normal (default);
