@@ -11,9 +11,16 @@ HBM:
              step through consecutive layers); the same rotation at M=16
              and M=128
   w4a4       quantize X (4096 x 8192 fp32) with X.U (rank 32), then the
-             block-scaled GEMM against pre-quantized W (8192 x 8192) + XU.V + b
+             block-scaled GEMM against W (8192 x 8192) quantized and
+             prepared once, as inference weights are + XU.V + b
 L2 is flushed (a 256 MiB write) before every op; every op's working set is
 also larger than L2.
+
+After the timed step, `sweep` times the square GEMMs at N = 512 ... 4096
+(the INT8 512 and INT4 2048 workloads among them) back to back, L2-hot
+where the working set fits in L2 and marked so; `cpu_baseline.per_config`
+times the oracle per workload (in full where it finishes in seconds, else on
+a 256-row sample, extrapolated to the whole problem and marked so).
 
 Headline `value`: INT8 GEMM TOPS at N=8192 (2*N^3 / time of qgemm_s8,
 including its operand conversion).  `breakdown` holds every op's throughput
@@ -47,7 +54,8 @@ FP8_RATIO, FP4_RATIO = 2.0, 6.0
 # DRAM bytes (read + write) of one qgemm_s8 main-kernel launch at 8192^3, from
 # Nsight Compute (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # measured for the current kernel (the capture command is in the profiles).
-S8_MAIN_DRAM_BYTES = 1104459776 + 253241856
+S8_MAIN_DRAM_BYTES = None
+S8_TRAFFIC_SOURCE = None
 
 # Performance-regression floors: (breakdown entry, key) -> lowest accepted
 # fraction of its peak, about 15% under what GB300 measures.  The line
@@ -59,13 +67,17 @@ FLOORS = {
     ("w4a16_m1_4096", "frac_of_hbm"): 0.32,
     ("w4a16_m16_4096", "frac_of_hbm"): 0.18,
     ("w4a16_m128_4096", "frac_of_hbm"): 0.10,
-    ("w4a4_4096x8192x8192_r32", "frac_of_f16_peak"): 0.31,
+    ("w4a4_4096x8192x8192_r32", "frac_of_fp8_peak"): 0.16,
 }
+
+# Square sweep sizes measured after the step (8192 is the step itself).
+SWEEP_N = (512, 1024, 2048, 4096)
 
 # One-knob ablations (--ablate NAME): the library setter, the values tried
 # (the default first) and the ops whose speed the knob can change.
 ABLATIONS = {
     "gemm_path": ("qg_set_gemm_path", (0, 1, 2), ("s8", "s4", "f16", "w4a4_gemm")),
+    "w4a4_tile": ("qg_set_w4a4_pair_form", (0, 1), ("w4a4_gemm",)),
     "pdl": ("qg_set_pdl", (1, 0), ("w4a16", "w4a16_m16", "w4a16_m128")),
     "s8_chunk": ("qg_set_s8_chunk", (16, 8, 4), ("s8",)),
     "l2_policy": ("qg_set_l2_policy", (0, 1, 2), ("s8", "s4", "f16")),
@@ -296,23 +308,25 @@ class Workload:
         return 1
 
     def w4a4_gemm(self):
-        q, s, xu = self.q_out
-        self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, Vt=self.Vt, bias=self.bias,
-                          Y=self.Y4, ws=self.ws_w4)
-        return 4  # operand expansion, two scale transposes, GEMM
-
-    def w4a4_gemm_prepacked(self):
+        """The GEMM against weights prepared once (w4a4_prepack_weights)."""
         q, s, xu = self.q_out
         self.qg.w4a4_gemm_prepacked(q, s, self.packed_w4, W4_N, W4_K, XU=xu, Vt=self.Vt, bias=self.bias,
                                     Y=self.Y4, ws=self.ws_w4p)
         return 3  # X operand expansion, X scale transpose, GEMM
+
+    def w4a4_gemm_unprepared(self):
+        """The same GEMM from the quantized weights, converted on every call."""
+        q, s, xu = self.q_out
+        self.qg.w4a4_gemm(q, s, self.qw, self.sw, W4_K, XU=xu, Vt=self.Vt, bias=self.bias,
+                          Y=self.Y4, ws=self.ws_w4)
+        return 4  # operand expansion, two scale transposes, GEMM
 
     def flush(self):
         self.flush_buf.fill_(1)
 
 
 WORKLOAD = ("INT8/INT4/FP16 GEMM 8192^3, W4A16 M=1/16/128 N=K=4096 g128, "
-            "W4A4 4096x8192x8192 r32 (one step = all eight ops)")
+            "W4A4 4096x8192x8192 r32, weights prepared once (one step = all eight ops)")
 OPS = ["s8", "s4", "f16", "w4a16", "w4a16_m16", "w4a16_m128", "w4a4_quant", "w4a4_gemm"]
 MAIN_KERNEL_OPS = {"s8", "s4", "f16", "w4a4_gemm"}  # ops with a timed tcgen05 GEMM kernel
 
@@ -380,27 +394,29 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop(w0, w1)
     assert qg.device_status() == qg.QG_OK, "device-side wait timed out in the timed region"
 
-    # W4A4 with prepacked weights: timed after the step, same flush and events
-    pre = []
+    # W4A4 with the weights converted on every call: timed after the step,
+    # same flush and events
+    unp = []
     for i in range(-max(args.warmup, 0), min(args.steps, 50)):
         wl.flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        wl.w4a4_gemm_prepacked()
+        wl.w4a4_gemm_unprepared()
         b.record(stream)
         if i >= 0:
-            pre.append((a, b))
+            unp.append((a, b))
     torch.cuda.synchronize()
-    w4_pre_ms = statistics.median(a.elapsed_time(b) for a, b in pre)
+    w4_unp_ms = statistics.median(a.elapsed_time(b) for a, b in unp)
+    peaks, peak_src = load_peaks()
+    bf16 = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    sweep = measure_sweep(wl, stream, bf16, steps=max(5, min(args.steps, 30)), warmup=max(args.warmup, 1))
 
     t_op = {op: [a.elapsed_time(b) for a, b in ev[op]] for op in OPS}          # ms
     t_k = {op: [a.elapsed_time(b) for a, b in kev[op]] for op in MAIN_KERNEL_OPS}
     step_ms = [sum(t_op[op][i] for op in OPS) for i in range(args.steps)]
     total_ms, s8_ms = replica_times(dist, dev, sum(step_ms), sum(t_op["s8"]))
 
-    peaks, peak_src = load_peaks()
-    bf16 = float(peaks["bf16_tflops"])
-    hbm = float(peaks["hbm_gbs"])
     med = {op: statistics.median(v) for op, v in t_op.items()}
     medk = {op: statistics.median(v) for op, v in t_k.items()}
     gemm_ops = 2.0 * N_SQ ** 3
@@ -440,16 +456,18 @@ def run_ours(args, rank, world, local_rank):
             "quantize_us": round(med["w4a4_quant"] * 1e3, 1),
             "quantize_GB/s": round(W4_M * W4_K * 4 / (med["w4a4_quant"] * 1e-3) / 1e9, 1),
             "gemm_us": round(med["w4a4_gemm"] * 1e3, 1),
+            "gemm": "w4a4_gemm_prepacked: weights prepared once by w4a4_prepack_weights; per call "
+                    "the X operand conversion, its scale table and the GEMM kernel",
             "TOPS": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]), 1),
             "kernel_TOPS": round(tops(w4_ops, medk["w4a4_gemm"]), 1),
             "mma_kind": "f8f6f4 e4m3 exact 64-block partials, scales applied in fp32",
-            "frac_of_f16_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"]) / bf16, 3),
+            "frac_of_fp8_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"])
+                                      / (FP8_RATIO * bf16), 3),
+            "kernel_frac_of_fp8_peak": round(tops(w4_ops, medk["w4a4_gemm"]) / (FP8_RATIO * bf16), 3),
             "mfu_vs_fp4_peak": round(tops(w4_ops, med["w4a4_quant"] + med["w4a4_gemm"])
                                      / (FP4_RATIO * bf16), 3),
-            "gemm_prepacked_us": round(w4_pre_ms * 1e3, 1),
-            "TOPS_prepacked": round(tops(w4_ops, med["w4a4_quant"] + w4_pre_ms), 1),
-            "prepacked": "w4a4_gemm_prepacked, weights converted once by w4a4_prepack_weights "
-                         "(timed after the step, not part of it)"},
+            "gemm_unprepared_us": round(w4_unp_ms * 1e3, 1),
+            "unprepared": "w4a4_gemm (weights converted on every call), timed after the step"},
         "op_ms_median": {op: round(v, 4) for op, v in med.items()},
     }
     k_ms = medk["s8"]
@@ -459,8 +477,12 @@ def run_ours(args, rank, world, local_rank):
                 "achieved": round(achieved, 1), "peak": bf16, "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 dense (fp16 kind runs at the bf16 rate)",
                 "frac": round(achieved / bf16, 3), "traffic": S8_MAIN_DRAM_BYTES,
-                "traffic_unit": "bytes per launch (DRAM read + write, one Nsight Compute capture)",
-                "algorithmic_bytes": 2 * 2 * N_SQ * N_SQ + 4 * N_SQ * N_SQ}
+                "traffic_unit": "bytes per launch (DRAM read + write, Nsight Compute; see traffic_source)",
+                "traffic_source": S8_TRAFFIC_SOURCE,
+                # the method's bytes: int8 A and B in, int32 C out
+                "algorithmic_bytes": 2 * N_SQ * N_SQ + 4 * N_SQ * N_SQ,
+                # what this kernel must move at least: its fp16 copies of A and B, int32 C
+                "kernel_operand_bytes": 2 * 2 * N_SQ * N_SQ + 4 * N_SQ * N_SQ}
 
     result = {
         "metric": METRIC, "value": round(s8_tops, 1), "unit": "TOPS", "n_gpus": world,
@@ -471,13 +493,14 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "256 MiB write before every op; every working set > L2",
                    "wall_s_timed_region": round(wall, 3)},
-        "breakdown": breakdown, "roofline": roofline, "clocks": clk,
+        "breakdown": breakdown, "sweep": sweep, "roofline": roofline, "clocks": clk,
         "gpu_launches": launches, "floors": check_floors(breakdown),
     }
     if rank == 0 and args.e2e:
         result["e2e"] = measure_e2e(wl, args)
     if rank == 0 and world == 1 and args.cpu_baseline:
         result["cpu_baseline"] = oracle_baseline(args.cpu_seconds)
+        result["cpu_baseline"]["per_config"] = oracle_per_config()
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -560,6 +583,125 @@ def measure_e2e(wl, args):
                   "conversion + GEMM and copy-out overlapped on the library's three streams)"}
 
 
+def sweep_working_set(op: str, n: int) -> int:
+    """Bytes one call touches in HBM/L2: inputs, output and the converted
+    operand copies it writes and reads."""
+    if op == "s8":
+        return 2 * n * n + 4 * n * n + 2 * 2 * n * n
+    if op == "s4":
+        return n * n + 4 * n * n + 2 * n * n
+    return 2 * 2 * n * n + 2 * n * n
+
+
+def measure_sweep(wl, stream, bf16: float, steps: int = 30, warmup: int = 3,
+                  sizes=SWEEP_N) -> dict:
+    """The square GEMMs at the sweep sizes: back to back (no flush), median
+    of `steps` calls, the whole call and its main kernel (library-recorded
+    events).  A size whose working set fits in L2 is reported L2-hot."""
+    import numpy as np
+    import torch
+    from bit_quantized_tensor_gb300 import inputs
+    qg, dev = wl.qg, wl.dev
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak = {"s8": bf16, "s4": FP8_RATIO * bf16, "f16": bf16}
+    kind = {"s8": "f16", "s4": "fp8", "f16": "f16"}
+    out = {}
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    for n in sizes:
+        A8, B8 = t(inputs.s8_uniform(n, n, 1002)), t(inputs.s8_uniform(n, n, 2002))
+        A4, B4 = t(inputs.s4_packed_uniform(n, n, 1002)), t(inputs.s4_packed_uniform(n, n, 2002))
+        Af, Bf = t(inputs.f16_normal(n, n, 1002)), t(inputs.f16_normal(n, n, 2002))
+        C32 = torch.empty((n, n), dtype=torch.int32, device=dev)
+        C16 = torch.empty((n, n), dtype=torch.float16, device=dev)
+        ws8 = torch.empty(qg.workspace_size(qg.QG_OP_S8, n, n, n), dtype=torch.uint8, device=dev)
+        ws4 = torch.empty(qg.workspace_size(qg.QG_OP_S4, n, n, n), dtype=torch.uint8, device=dev)
+        calls = {"s8": lambda: qg.qgemm_s8(A8, B8, C=C32, ws=ws8),
+                 "s4": lambda: qg.qgemm_s4(A4, B4, n, C=C32, ws=ws4),
+                 "f16": lambda: qg.gemm_f16(Af, Bf, C=C16)}
+        for op, fn in calls.items():
+            evs = []
+            for i in range(-warmup, steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ka.record(stream)
+                kb.record(stream)
+                qg.lib().qg_set_profile_events(ka.cuda_event, kb.cuda_event)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                qg.lib().qg_set_profile_events(None, None)
+                if i >= 0:
+                    evs.append((a, b, ka, kb))
+            torch.cuda.synchronize()
+            ms = statistics.median(a.elapsed_time(b) for a, b, _, _ in evs)
+            kms = statistics.median(ka.elapsed_time(kb) for _, _, ka, kb in evs)
+            ops = 2.0 * n ** 3
+            ws = sweep_working_set(op, n)
+            out[f"{'int8' if op == 's8' else 'int4' if op == 's4' else 'fp16'}_{n}"] = {
+                "TOPS" if op != "f16" else "TFLOPS": round(ops / ms / 1e9, 1),
+                "kernel_TOPS": round(ops / kms / 1e9, 1),
+                f"frac_of_{kind[op]}_peak": round(ops / ms / 1e9 / peak[op], 3),
+                f"kernel_frac_of_{kind[op]}_peak": round(ops / kms / 1e9 / peak[op], 3),
+                "us": round(ms * 1e3, 2), "working_set_bytes": ws,
+                "l2": "hot (working set fits in L2, back-to-back calls)" if ws <= l2
+                      else "working set larger than L2 (back-to-back calls)"}
+        del A8, B8, A4, B4, Af, Bf, C32, C16, ws8, ws4
+    assert qg.device_status() == qg.QG_OK, "device-side wait timed out in the sweep"
+    return out
+
+
+def oracle_per_config() -> dict:
+    """The CPU oracle timed per workload on the host cores: in full where it
+    finishes in seconds (INT8 512, INT4 2048, the sweep up to 2048, W4A16 at
+    M = 1, 16, 128), on the first rows of the output otherwise (N = 4096 and
+    8192: 128 rows of the integer GEMMs, 32 of the fp64 FP16 GEMM; 64 rows of
+    the W4A4 GEMM), with the time for the whole problem extrapolated linearly
+    in rows and marked so.  About 15 s of host time in all."""
+    import oracle
+    from bit_quantized_tensor_gb300 import inputs
+    oracle.build()
+    res = {}
+
+    def timed(label, ops, rows_done, rows_all, fn, unit="TOPS"):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        full = dt * rows_all / rows_done
+        res[label] = {"seconds": round(dt, 3), "rows": rows_done, "of_rows": rows_all,
+                      "extrapolated": rows_done < rows_all,
+                      "seconds_whole_problem": round(full, 2),
+                      unit: round(ops / full / 1e12, 6)}
+
+    for n in SWEEP_N + (N_SQ,):
+        r = n if n <= 2048 else 128
+        A8, B8 = inputs.s8_uniform(r, n, 1002), inputs.s8_uniform(n, n, 2002)
+        timed(f"int8_{n}", 2.0 * n ** 3, r, n, lambda: oracle.gemm_s8(A8, B8))
+        A4, B4 = inputs.s4_packed_uniform(r, n, 1002), inputs.s4_packed_uniform(n, n, 2002)
+        timed(f"int4_{n}", 2.0 * n ** 3, r, n, lambda: oracle.gemm_s4(A4, B4, n))
+        r = n if n <= 2048 else 32
+        Af, Bf = inputs.f16_normal(r, n, 1002), inputs.f16_normal(n, n, 2002)
+        timed(f"fp16_{n}", 2.0 * n ** 3, r, n, lambda: oracle.gemm_f16(Af, Bf), unit="TFLOPS")
+    W = inputs.s4_packed_uniform(W16_N, W16_K, 2003)
+    S = inputs.f16_uniform(W16_N, W16_K // 128, 0.005, 0.02, 3003)
+    for m in W16_MS:
+        X = inputs.f16_normal(m, W16_K, 1003)
+        timed(f"w4a16_m{m}_4096", 2.0 * m * W16_N * W16_K, m, m, lambda: oracle.w4a16(X, W, S, 128))
+    r = 64
+    X4 = inputs.f32_normal(r, W4_K, 1004)
+    qx, sx = oracle.w4a4_quantize(X4, 64)
+    qw, sw = oracle.w4a4_quantize(inputs.f32_normal(W4_N, W4_K, 2004), 64)
+    U = inputs.f16_normal(W4_K, W4_R, 3004, sigma=0.02)
+    V = inputs.f16_normal(W4_R, W4_N, 3005, sigma=0.02)
+    b = inputs.f16_normal(1, W4_N, 3006, sigma=0.1)[0]
+    xu = oracle.lowrank_xu(X4, U)
+    timed("w4a4_4096x8192x8192_r32", 2.0 * W4_M * W4_N * W4_K + 2.0 * W4_M * W4_N * W4_R, r, W4_M,
+          lambda: oracle.w4a4_gemm(qx, sx, qw, sw, 64, W4_K, XU=xu, V=V, bias=b))
+    return {"cores": oracle.threads(), "kind": "oracle", "configs": res}
+
+
 def oracle_operands():
     """The seeded 8192^3 INT8 operands of the headline GEMM (host arrays)."""
     from bit_quantized_tensor_gb300 import inputs
@@ -631,7 +773,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
                     help="target CPU seconds of the oracle baseline sample")
     ap.add_argument("--check-floors", action="store_true",
                     help="exit 1 when an op falls under its regression floor")

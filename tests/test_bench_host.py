@@ -34,3 +34,20 @@ def test_ablation_knobs_name_library_setters_and_known_ops():
         assert setter in qg.SIGNATURES, name
         assert len(values) >= 2 and len(set(values)) == len(values), name
         assert set(ops) <= set(bench.OPS), name
+
+
+def test_sweep_working_sets_and_l2_labels():
+    # int8: A, B (1 B each), C (4 B), fp16 copies of A and B (2 B each)
+    assert bench.sweep_working_set("s8", 512) == (2 + 4 + 4) * 512 * 512
+    # int4: packed A, B (n^2 bytes together), C, e4m3 copies (1 B each)
+    assert bench.sweep_working_set("s4", 2048) == (1 + 4 + 2) * 2048 * 2048
+    assert bench.sweep_working_set("f16", 4096) == 6 * 4096 * 4096
+    # the two small workload definitions fit in a 126 MiB L2, 4096^3 INT8 does not
+    l2 = 126 << 20
+    assert bench.sweep_working_set("s8", 512) <= l2 and bench.sweep_working_set("s4", 2048) <= l2
+    assert bench.sweep_working_set("s8", 4096) > l2
+
+
+def test_w4a4_floor_is_against_the_fp8_kind():
+    keys = [k for (e, k) in bench.FLOORS if e.startswith("w4a4")]
+    assert keys == ["frac_of_fp8_peak"]
