@@ -54,8 +54,9 @@ FP8_RATIO, FP4_RATIO = 2.0, 6.0
 # DRAM bytes (read + write) of one qgemm_s8 main-kernel launch at 8192^3, from
 # Nsight Compute (dram__bytes_read.sum + dram__bytes_write.sum); None until
 # measured for the current kernel (the capture command is in the profiles).
-S8_MAIN_DRAM_BYTES = None
-S8_TRAFFIC_SOURCE = None
+S8_MAIN_DRAM_BYTES = 2 * (531950336 + 118928384)
+S8_TRAFFIC_SOURCE = ("one launch at 4096x8192x8192 (-k tc_gemm2 -c 1), read + write bytes scaled by "
+                     "the tile count (x2) to 8192^3 (the tc_gemm2 traffic summary under profiles/)")
 
 # Performance-regression floors: (breakdown entry, key) -> lowest accepted
 # fraction of its peak, about 15% under what GB300 measures.  The line
@@ -410,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     bf16 = float(peaks["bf16_tflops"])
     hbm = float(peaks["hbm_gbs"])
-    sweep = measure_sweep(wl, stream, bf16, steps=max(5, min(args.steps, 30)), warmup=max(args.warmup, 1))
+    sweep = (measure_sweep(wl, stream, bf16, steps=max(5, min(args.steps, 30)), warmup=max(args.warmup, 1))
+             if args.sweep else None)
 
     t_op = {op: [a.elapsed_time(b) for a, b in ev[op]] for op in OPS}          # ms
     t_k = {op: [a.elapsed_time(b) for a, b in kev[op]] for op in MAIN_KERNEL_OPS}
@@ -773,6 +775,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the square-GEMM sweep after the step (e.g. for a launch list of the step)")
     ap.add_argument("--cpu-seconds", type=float, default=6.0,
                     help="target CPU seconds of the oracle baseline sample")
     ap.add_argument("--check-floors", action="store_true",

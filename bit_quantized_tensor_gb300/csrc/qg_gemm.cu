@@ -398,11 +398,11 @@ int conv_grid(int dev, int64_t work_items) {
 
 // Chunk length (in k-blocks of 64) of the exact int8 path; <= 16 keeps
 // every fp32 partial sum within 2^24.  Adjustable for tests.
-static int g_s8_chunk_kb = 16;
+static std::atomic<int> g_s8_chunk_kb{16};  // qg_set_s8_chunk; read once per call
 
 int run_gemm_s8_converted(const __half* A16, const __half* B16, int64_t M, int64_t N, int64_t K, int32_t* C,
                           int64_t ldc, const Ctl& ctl, cudaStream_t stream) {
-    return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc, g_s8_chunk_kb, nullptr,
+    return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc, g_s8_chunk_kb.load(), nullptr,
                                                ctl, stream);
 }
 
@@ -461,7 +461,7 @@ int qg_set_l2_policy(int mode) {
 
 int qg_set_s8_chunk(int kblocks) {
     if (kblocks < 1 || kblocks > 16) return QG_ERR_INVALID_ARG;
-    g_s8_chunk_kb = kblocks;
+    g_s8_chunk_kb.store(kblocks);
     return QG_OK;
 }
 
@@ -513,7 +513,7 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K, const int8_t* A, int64_t lda, int 
     int rc = launch_expand<S8ToF16>(jobs, 2, K / 16, dev, s);
     if (rc) return rc;
     return launch_gemm<MmaKind::F16, Epi::S32>(A16, K * 2, B16, K * 2, M, N, K, C, ldc,
-                                               g_s8_chunk_kb, nullptr, ctl, s);
+                                               g_s8_chunk_kb.load(), nullptr, ctl, s);
 }
 
 int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_bytes, int layout_a,

@@ -17,6 +17,10 @@
 //  - the first call on each device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
 //    first call before any stream capture on the device;
+//  - the stream must belong to the current device (checked: the cached
+//    address is that device's); the cache lives as long as the library and
+//    is not refreshed if a device is reset (cudaDeviceReset), so the library
+//    must not be used on a device after that device was reset;
 //  - every call shares the one array and it keeps the last call's contents.
 //    Nothing in it has to start at zero (each call overwrites the part it
 //    reads first), but calls that overlap on the GPU (different streams, or
@@ -62,6 +66,16 @@ extern "C" int qgemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t* A
     if (need == 0 || need > kScratchBytes) return QG_ERR_WORKSPACE;
     const int dev = qg::current_device();
     if (dev < 0 || dev >= kMaxDevices) return QG_ERR_CUDA;
+    if (stream) {
+        // the scratch address is per device: a stream of another device would
+        // run the kernels against the wrong device's array
+        int sdev = -1;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+            cudaGetLastError();
+            return QG_ERR_INVALID_ARG;
+        }
+        if (sdev != dev) return QG_ERR_INVALID_ARG;
+    }
     void* scratch = nullptr;
     const int rc = scratch_address(dev, &scratch);
     if (rc != QG_OK) return rc;

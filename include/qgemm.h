@@ -35,6 +35,10 @@
  *    nothing is enqueued.  A launch failure returns QG_ERR_CUDA.  Kernels bound
  *    every wait; a wait that runs out records QG_ERR_TIMEOUT in a device
  *    status word that qg_device_status() reports.  No call traps or aborts.
+ *  - Per-device state (the status word's address, the no-alloc scratch
+ *    address) is looked up once per device and kept for the life of the
+ *    library: do not use the library on a device after cudaDeviceReset of
+ *    that device in the same process.
  */
 #ifndef QGEMM_H
 #define QGEMM_H
@@ -224,6 +228,9 @@ int qgemm_s8(int64_t M, int64_t N, int64_t K,
  *    QG_ERR_WORKSPACE and enqueue nothing;
  *  - the first call on each device looks up the array's device address with
  *    that device current; make it before any stream capture on the device;
+ *  - `stream` must belong to the current device (QG_ERR_INVALID_ARG
+ *    otherwise); the looked-up address is kept for the life of the library,
+ *    so do not call it on a device after cudaDeviceReset of that device;
  *  - all calls share the array and it keeps the last call's contents; no part
  *    of it needs to start at zero, but calls that overlap on the GPU (other
  *    streams, unordered host threads) race on it: serialize them.

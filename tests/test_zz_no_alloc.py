@@ -25,6 +25,14 @@ def _raw_call(A, B, C, stream):
                                      C.data_ptr(), C.stride(0), stream)
 
 
+def test_scratch_need_at_the_documented_limit():
+    # M = N = K = 2048 needs exactly the 16 MiB the array holds (two fp16
+    # operand copies of 8 MiB each); K = 2064 needs 16 MiB + 128 KiB
+    need = qg.lib().qg_workspace_size(qg.QG_OP_S8, 2048, 2048, 2048)
+    assert need == 16 << 20
+    assert qg.lib().qg_workspace_size(qg.QG_OP_S8, 2048, 2048, 2064) > 16 << 20
+
+
 def test_rejects_problems_beyond_the_static_scratch():
     # 2*K*(M+N) = 2*4096*8192 = 64 MiB > 16 MiB: refused before any GPU work
     L = qg.lib()
@@ -50,4 +58,27 @@ def test_matches_qgemm_s8_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         got, want = C.cpu().numpy(), ref.cpu().numpy()
         assert np.array_equal(got, want), f"call {i}: noalloc result differs from qgemm_s8"
+    assert qg.device_status() == qg.QG_OK
+
+
+@pytest.mark.gpu
+def test_the_largest_accepted_and_the_smallest_refused_problem():
+    import torch
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream().cuda_stream
+    # exactly the array's size: accepted, bit-exact against qgemm_s8
+    A = torch.from_numpy(inputs.s8_uniform(2048, 2048, 7100)).to(dev)
+    B = torch.from_numpy(inputs.s8_uniform(2048, 2048, 8100)).to(dev)
+    C = torch.full((2048, 2048), -1, dtype=torch.int32, device=dev)
+    assert _raw_call(A, B, C, stream) == qg.QG_OK
+    ref = qg.qgemm_s8(A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(C, ref)
+    # 16 more k values: refused before anything is enqueued, C untouched
+    A2 = torch.from_numpy(inputs.s8_uniform(2048, 2064, 7101)).to(dev)
+    B2 = torch.from_numpy(inputs.s8_uniform(2048, 2064, 8101)).to(dev)
+    C2 = torch.full((2048, 2048), 12345, dtype=torch.int32, device=dev)
+    assert _raw_call(A2, B2, C2, stream) == qg.QG_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((C2 == 12345).all())
     assert qg.device_status() == qg.QG_OK
