@@ -71,6 +71,7 @@ SIGNATURES = {
     "qg_kernel_budget_measure": (_int, [_int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "qg_set_s8_chunk": (_int, [_int]),
     "qg_set_gemm_path": (_int, [_int]),
+    "qg_set_s4_path": (_int, [_int]),
     "qg_set_w4a4_pair_form": (_int, [_int]),
     "qg_set_l2_policy": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),

@@ -19,6 +19,7 @@
 
 #include "qg_gemm_host.h"
 #include "tc_gemm2.cuh"
+#include "tc_gemm2_s4raw.cuh"
 
 namespace qg {
 
@@ -200,6 +201,51 @@ static int launch_gemm(const void* A, int64_t lda_bytes, const void* B, int64_t 
                                             bias, ctl, stream);
     return launch_tc<TcGemmCfg<KIND, EPI>>(A, lda_bytes, B, ldb_bytes, M, N, K, C, ldc, chunk_kb,
                                           bias, ctl, stream);
+}
+
+// qgemm_s4 route (qg_set_s4_path): 0 = the in-kernel nibble conversion where
+// it applies (CTA pairs, K <= 65536), 1 = always the conversion pre-pass.
+static std::atomic<int> g_s4_path{0};
+
+// INT4 GEMM straight from the packed operands (tc_gemm2_s4raw_kernel).
+static int launch_s4raw(const uint8_t* A, int64_t lda_bytes, const uint8_t* B, int64_t ldb_bytes, int64_t M,
+                        int64_t N, int64_t K, int32_t* C, int64_t ldc, const Ctl& ctl, cudaStream_t stream) {
+    using Cfg = S4RawCfg;
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return QG_ERR_CUDA;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!attr_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(tc_gemm2_s4raw_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return map_cuda(e);
+            attr_set[dev] = true;
+        }
+    }
+    S4RawParams p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
+    p.A = A;
+    p.B = B;
+    p.lda = lda_bytes;
+    p.ldb = ldb_bytes;
+    p.C = C;
+    p.ldc = ldc;
+    p.ctl = ctl;
+    const int64_t tiles = ((M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((N + Cfg::BN - 1) / Cfg::BN);
+    const int64_t max_pairs = num_sms(dev) / 2;
+    const int grid = 2 * static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    void *pb = nullptr, *pa = nullptr;
+    profile_events(&pb, &pa);
+    if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), stream) != cudaSuccess) return QG_ERR_CUDA;
+    tc_gemm2_s4raw_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(p);
+    int rc = map_cuda(cudaGetLastError());
+    if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), stream) != cudaSuccess) return QG_ERR_CUDA;
+    return rc;
 }
 
 int run_gemm_f16_tc(const __half* A, int64_t lda, const __half* B, int64_t ldb, int64_t M, int64_t N,
@@ -429,6 +475,8 @@ QG_TC_BUDGET(Tc2S8, "tc_gemm2_kernel<F16,S32>", 2);
 QG_TC_BUDGET(Tc2S4, "tc_gemm2_kernel<F8F6F4,S32>", 2);
 QG_TC_BUDGET(Tc2F16, "tc_gemm2_kernel<F16,F16>", 2);
 #undef QG_TC_BUDGET
+QG_KERNEL_BUDGET("tc_gemm2_s4raw_kernel", reinterpret_cast<const void*>(tc_gemm2_s4raw_kernel), S4RawCfg::THREADS,
+                 S4RawCfg::SMEM_BYTES, S4RawCfg::TMEM_COLS, 2, 1);
 QG_KERNEL_BUDGET("k_expand<S8ToF16>", reinterpret_cast<const void*>(k_expand<S8ToF16>), 256, 0, 0, 1, 1);
 QG_KERNEL_BUDGET("k_expand<S4ToE4M3>", reinterpret_cast<const void*>(k_expand<S4ToE4M3>), 256, 0, 0, 1, 1);
 
@@ -450,6 +498,12 @@ int qg_set_profile_events(void* before, void* after) {
 int qg_set_gemm_path(int path) {
     if (path < 0 || path > 2) return QG_ERR_INVALID_ARG;
     g_gemm_path.store(path);
+    return QG_OK;
+}
+
+int qg_set_s4_path(int path) {
+    if (path < 0 || path > 1) return QG_ERR_INVALID_ARG;
+    g_s4_path.store(path);
     return QG_OK;
 }
 
@@ -536,6 +590,11 @@ int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_byte
     if (!ctl.status) return QG_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    // the in-kernel conversion saves a launch and a pass over the operands;
+    // its transform is load/store-pipe bound, so large problems keep the
+    // TMA-fed kernel behind the pre-pass
+    if (g_s4_path.load() == 0 && use_pairs(M, N) && K <= S4RawCfg::MAX_K && M * N * K <= (int64_t(1) << 34))
+        return launch_s4raw(A, lda_bytes, B, ldb_bytes, M, N, K, C, ldc, ctl, s);
     uint8_t* A8 = static_cast<uint8_t*>(ws);
     uint8_t* B8 = static_cast<uint8_t*>(ws) + ((static_cast<size_t>(M) * K + 255) & ~size_t(255));
     const ExpandJob jobs[2] = {{A, M, lda_bytes, A8, K}, {B, N, ldb_bytes, B8, K}};

@@ -78,6 +78,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait with acquire semantics at cluster scope: for a phase
+// completed by arrivals (with release at cluster scope) from the other CTA of
+// the pair, whose earlier shared-memory stores must be visible after the wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with parity `parity` of barrier `bar` has completed.
 // Returns false (after recording QG_ERR_TIMEOUT with the call-site tag) when
 // the limit runs out, or when another role of this CTA has already set
@@ -98,11 +113,40 @@ static __device__ __noinline__ bool bounded_wait_slow(uint32_t bar, uint32_t par
     return false;
 }
 
+static __device__ __noinline__ bool bounded_wait_cluster_slow(uint32_t bar, uint32_t parity,
+                                                              volatile int* abort_flag, const Ctl& ctl,
+                                                              int site) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < kMaxWaitIterations; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (global_timer_ns() - t0 > ctl.timeout_ns) break;
+        }
+    }
+    if (abort_flag) *abort_flag = 1;
+    report_error(ctl, QG_ERR_TIMEOUT, site, bar, parity);
+    return false;
+}
+
+// bounded_wait with cluster-scope acquire (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     const Ctl& ctl, int site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return bounded_wait_cluster_slow(bar, parity, abort_flag, ctl, site);
+}
+
 // Inline fast path: one try_wait; the bounded loop only when not yet ready.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              const Ctl& ctl, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     return bounded_wait_slow(bar, parity, abort_flag, ctl, site);
+}
+
+// Orders this thread's shared-memory writes before later reads by the async
+// proxy (the tensor core's operand fetch).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // -------------------------------------------------------------------- TMA
@@ -344,6 +388,25 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
+}
+
+// Bulk copy of `bytes` bytes from this CTA's shared memory to the shared
+// memory of either CTA of the pair, completion signalled as transaction bytes
+// on `cluster_bar` (an mbarrier of the destination CTA).  Addresses 16-byte
+// aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2s_cluster(uint32_t cluster_dst, uint32_t src, uint32_t bytes,
+                                                      uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            cluster_dst),
+        "r"(src), "r"(bytes), "r"(cluster_bar)
+        : "memory");
+}
+
+// 32-bit store into the shared memory of either CTA of the pair (address from
+// mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // TMA 2-D load into this CTA's shared memory whose completion is signalled on

@@ -44,12 +44,6 @@
 
 namespace qg {
 
-// Orders this thread's shared-memory writes before later reads by the async
-// proxy (the tensor core's operand fetch).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Execution barrier over all threads of the cluster, without memory ordering.
 __device__ __forceinline__ void cluster_sync_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.aligned;" ::: "memory");

@@ -166,6 +166,13 @@ int qg_set_s8_chunk(int kblocks);
  * 2 = always CTA pairs.  Results are identical; only speed differs. */
 int qg_set_gemm_path(int path);
 
+/* Ablation knob: route of qgemm_s4.  0 = the GEMM kernel reads the packed
+ * nibbles and converts them itself where that is faster (CTA pairs, i.e.
+ * M >= 256 and N >= 256, K <= 65536 and M*N*K <= 2^34; default), 1 = always
+ * a conversion pass to e4m3 bytes in the workspace before the GEMM kernel.
+ * Results are identical; QG_ERR_INVALID_ARG for another value. */
+int qg_set_s4_path(int path);
+
 /* Ablation knob: tile of the paired kernel behind w4a4_gemm,
  * w4a4_gemm_affine and w4a4_gemm_prepacked when M > 128.  0 = 256 x 256
  * tiles with 16 epilogue warps (default), 1 = 256 x 192 tiles with 12.  The

@@ -291,3 +291,49 @@ def test_l2_policy_modes_same_results(dev, oracle, gemm_path, l2_policy, mode, p
     assert np.array_equal(C4, ref4), first_mismatch(C4, ref4)
     f1 = qg.gemm_f16(_t(Af, dev), _t(Bf, dev)).cpu().numpy()
     assert np.array_equal(f0.view(np.uint16), f1.view(np.uint16))
+
+
+# ------------------------------------- qgemm_s4: in-kernel conversion vs pre-pass
+
+@pytest.fixture
+def s4_path():
+    import bit_quantized_tensor_gb300 as qg
+    def set_path(p):
+        assert qg.lib().qg_set_s4_path(p) == 0
+    yield set_path
+    qg.lib().qg_set_s4_path(0)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("K", [1024, 65536])
+def test_qgemm_s4_extremes_on_pairs(dev, gemm_path, s4_path, path, K):
+    # -8 and 7 in every combination; K = 65536 is the largest K the in-kernel
+    # conversion takes (its fp32 partial sums reach 225 K = 14.7e6 < 2^24)
+    gemm_path(2)
+    s4_path(path)
+    A = np.full((512, K // 2), 0x88, dtype=np.uint8)   # rows 0..255: -8
+    A[256:] = 0x77                                      # rows 256..511: 7
+    B = np.full((512, K // 2), 0x88, dtype=np.uint8)
+    B[256:] = 0x77
+    C = _s4(dev, A, B, K)
+    assert np.all(C[:256, :256] == 64 * K) and np.all(C[256:, 256:] == 49 * K)
+    assert np.all(C[:256, 256:] == -56 * K) and np.all(C[256:, :256] == -56 * K)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("M,N,K", PATH_SHAPES + [(513, 777, 4160), (256, 512, 65568)])
+def test_qgemm_s4_routes_on_pairs(dev, oracle, gemm_path, s4_path, path, M, N, K):
+    # every shape on CTA pairs with either route; K = 65568 is past the
+    # in-kernel conversion's limit, so route 0 falls back to the pre-pass
+    gemm_path(2)
+    s4_path(path)
+    A = inputs.s4_packed_uniform(M, K, 1800 + M)
+    B = inputs.s4_packed_uniform(N, K, 2800 + N)
+    C = _s4(dev, A, B, K)
+    if K > 8192:
+        rows = inputs.sample_rows(M, 16, 4300 + M)
+        ref = oracle.gemm_s4(A[rows], B, K)
+        assert np.array_equal(C[rows], ref), first_mismatch(C[rows], ref)
+    else:
+        ref = oracle.gemm_s4(A, B, K)
+        assert np.array_equal(C, ref), first_mismatch(C, ref)
