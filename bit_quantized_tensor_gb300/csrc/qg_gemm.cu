@@ -224,15 +224,19 @@ static int launch_s4raw(const uint8_t* A, int64_t lda_bytes, const uint8_t* B, i
             attr_set[dev] = true;
         }
     }
+    // the packed operands, 64 bytes (one 128-wide K stage) x the CTA's 128 rows per box
+    CUtensorMap ta, tb;
+    int rc0 = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, lda_bytes, Cfg::RAW_ROW, Cfg::BM,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!rc0)
+        rc0 = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, ldb_bytes, Cfg::RAW_ROW, Cfg::B_ROWS,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc0) return rc0;
     S4RawParams p;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.num_kb = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
-    p.A = A;
-    p.B = B;
-    p.lda = lda_bytes;
-    p.ldb = ldb_bytes;
     p.C = C;
     p.ldc = ldc;
     p.ctl = ctl;
@@ -242,7 +246,7 @@ static int launch_s4raw(const uint8_t* A, int64_t lda_bytes, const uint8_t* B, i
     void *pb = nullptr, *pa = nullptr;
     profile_events(&pb, &pa);
     if (pb && cudaEventRecord(static_cast<cudaEvent_t>(pb), stream) != cudaSuccess) return QG_ERR_CUDA;
-    tc_gemm2_s4raw_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(p);
+    tc_gemm2_s4raw_kernel<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(ta, tb, p);
     int rc = map_cuda(cudaGetLastError());
     if (!rc && pa && cudaEventRecord(static_cast<cudaEvent_t>(pa), stream) != cudaSuccess) return QG_ERR_CUDA;
     return rc;
@@ -590,9 +594,11 @@ int qgemm_s4(int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda_byte
     if (!ctl.status) return QG_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // the in-kernel conversion saves a launch and a pass over the operands;
-    // its transform is load/store-pipe bound, so large problems keep the
-    // TMA-fed kernel behind the pre-pass
+    // the in-kernel conversion saves a launch and a pass over the operands,
+    // but its transform warps (shared-memory reads, conversion, generic
+    // stores, the stage hand-off) pace its K loop at about 1.7x the MMA time
+    // of a stage: 2.13 against 3.67 POPS at 8192^3, so large problems keep
+    // the TMA-fed kernel behind the pre-pass
     if (g_s4_path.load() == 0 && use_pairs(M, N) && K <= S4RawCfg::MAX_K && M * N * K <= (int64_t(1) << 34))
         return launch_s4raw(A, lda_bytes, B, ldb_bytes, M, N, K, C, ldc, ctl, s);
     uint8_t* A8 = static_cast<uint8_t*>(ws);

@@ -23,22 +23,27 @@
 // values past the end of the matrix are written as u = 0 (zero products) and
 // left out of the sums.
 //
-// Roles (22 warps):
+// Roles (23 warps):
 //   warp 0       TMEM owner; lane 0 of the leader CTA issues the paired MMAs
-//   warps 1..16  transform: global -> registers -> e4m3 bytes in the 128-byte
-//                swizzled K-major stage, DEPTH stages of loads in flight per
-//                thread; row sums of the rows they convert
-//   warp 17      signaler: forwards each finished stage to the MMA
-//   warps 18..21 epilogue: TMEM -> registers, the correction, int32 stores
+//   warp 1       lane 0: TMA producer of the packed bytes (this CTA's 128 rows
+//                of A and of B per 128-wide K stage) into a RAW_STAGES ring
+//   warps 2..17  transform: packed bytes (shared memory) -> e4m3 bytes in the
+//                128-byte swizzled K-major MMA stage; row sums of the rows
+//                they convert
+//   warp 18      signaler: forwards each finished stage to the MMA
+//   warps 19..22 epilogue: TMEM -> registers, the correction, int32 stores
 //                (one warp per TMEM lane quadrant, all 256 columns; it runs
 //                once per tile, under the next tile's K loop)
+// The packed bytes come in by TMA rather than by per-thread global loads: a
+// global load costs the load/store pipe one wavefront per 32-byte sector,
+// a shared-memory read one per 128 bytes, and with global loads that pipe
+// was the bottleneck (1.95 POPS at 8192^3).
 // Synchronization:
+//   raw_full/    per CTA: the producer's TMA completes raw_full; the transform
+//   raw_empty    warps arrive on raw_empty once they have used the bytes
 //   slot s       named barrier 1 + s: the transform threads arrive (bar.arrive,
 //                after their stores and fence.proxy.async) and the signaler
-//                waits.  An mbarrier arrive with release semantics would wait
-//                for the arriving thread's prefetched global loads to complete,
-//                serializing every stage on a memory round trip; the signaler
-//                has no loads in flight.
+//                waits
 //   full[s]      leader only: armed by the leader's signaler (arrive with 32
 //                expected bytes); each CTA's signaler then issues a 16-byte
 //                shared-memory bulk copy into the leader that completes on it.
@@ -68,33 +73,35 @@ struct S4RawCfg {
     static constexpr int A_BYTES = BM * 128;
     static constexpr int B_BYTES = B_ROWS * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int RAW_A_BYTES = BM * RAW_ROW;      // packed bytes of a stage (A, B halves)
+    static constexpr int RAW_B_BYTES = B_ROWS * RAW_ROW;
+    static constexpr int RAW_BYTES = RAW_A_BYTES + RAW_B_BYTES;
+    static constexpr int STAGES = 5;                      // e4m3 MMA operand ring
+    static constexpr int RAW_STAGES = 4;                  // packed-byte ring
     static constexpr int SUMS_BYTES = (BM + BN) * 4;      // RA of this CTA's rows, RB of the tile
     static constexpr int SMEM_LIMIT = 232448;
     static constexpr int BARRIER_BYTES = 256;
     static constexpr int ALIGN_SLACK = 1024;
-    static constexpr int STAGES =
-        (SMEM_LIMIT - SUMS_BYTES - BARRIER_BYTES - ALIGN_SLACK) / STAGE_BYTES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + SUMS_BYTES + BARRIER_BYTES + ALIGN_SLACK;
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + RAW_STAGES * RAW_BYTES + SUMS_BYTES + BARRIER_BYTES + ALIGN_SLACK;
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = 512;
-    // warp 0 = TMEM owner / MMA issuer, then the transform warps (loads for
-    // DEPTH stages in flight per thread), then the epilogue warps
-    static constexpr int XF_WARP0 = 1, XF_WARPS = 16;
+    static constexpr int PROD_WARP = 1;
+    static constexpr int XF_WARP0 = 2, XF_WARPS = 16;
     static constexpr int SIG_WARP = XF_WARP0 + XF_WARPS;  // forwards each stage to the MMA
     static constexpr int EPI_WARP0 = SIG_WARP + 1, EPI_WARPS = 4;  // one per TMEM lane quadrant
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-    static constexpr int DEPTH = 3;
     static constexpr int XF_THREADS = 32 * XF_WARPS;
     // each transform thread: one 16-byte quarter of a 64-byte raw row segment
     static constexpr int ROW_SLOTS = XF_THREADS / 4;      // rows covered per pass
     static constexpr int A_TASKS = BM / ROW_SLOTS;        // A rows per thread per stage
     static constexpr int B_TASKS = B_ROWS / ROW_SLOTS;
     static constexpr int TASKS = A_TASKS + B_TASKS;
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * ACC_BUFS + 3;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * RAW_STAGES + 2 * ACC_BUFS + 3;
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, 2 * BM, BN);  // e4m3 x e4m3, M = 256
     static constexpr int64_t MAX_K = 65536;               // 225 * K < 2^24: exact fp32 sums
 
-    static_assert(STAGES >= 5, "operand ring too shallow");
+    static_assert(STAGES >= 4 && RAW_STAGES >= 3, "rings too shallow");
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared-memory budget exceeded");
     static_assert(2 * SMEM_BYTES > 233472, "one CTA per SM keeps all 512 TMEM columns free");
     static_assert(NUM_BARRIERS * 8 + 8 + 16 + 32 <= BARRIER_BYTES, "barrier area too small");
@@ -107,15 +114,15 @@ struct S4RawCfg {
 struct S4RawParams {
     int M, N, K;
     int num_kb;                 // ceil(K / 128)
-    const uint8_t* A;           // M x K/2 bytes, row stride lda bytes
-    const uint8_t* B;           // N x K/2 bytes, row stride ldb bytes
-    int64_t lda, ldb;
     int32_t* C;
     int64_t ldc;
     Ctl ctl;
 };
 
 enum S4RawSite : int {
+    kSiteS4Prod = 138,
+    kSiteS4XfRaw = 139,
+    kSiteS4Drain = 130,
     kSiteS4XfEmpty = 131,
     kSiteS4XfSums = 132,
     kSiteS4MmaAcc = 133,
@@ -133,15 +140,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// 16 packed bytes from global memory, read once (not kept in L1).
-__device__ __forceinline__ uint4 ld_raw16(const uint8_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // Eight packed nibbles -> the even ones (k = 0, 2, 4, 6) and the odd ones
 // (k = 1, 3, 5, 7) as offset-binary bytes u = n XOR 8.
 __device__ __forceinline__ void split_offset(uint32_t w, uint32_t& even, uint32_t& odd) {
@@ -150,7 +148,8 @@ __device__ __forceinline__ void split_offset(uint32_t w, uint32_t& even, uint32_
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1)
-    tc_gemm2_s4raw_kernel(const S4RawParams p) {
+    tc_gemm2_s4raw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const S4RawParams p) {
     using Cfg = S4RawCfg;
     constexpr int STAGES = Cfg::STAGES, ACC = Cfg::ACC_BUFS;
     extern __shared__ uint8_t smem_raw[];
@@ -158,7 +157,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-    int32_t* sRA = reinterpret_cast<int32_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint8_t* sRaw = smem + STAGES * Cfg::STAGE_BYTES;  // RAW_STAGES x (A rows, B rows) x 64 bytes
+    int32_t* sRA = reinterpret_cast<int32_t*>(sRaw + Cfg::RAW_STAGES * Cfg::RAW_BYTES);
     int32_t* sRB = sRA + Cfg::BM;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sRB + Cfg::BN);
     const uint32_t bar0 = smem_u32(bars);
@@ -166,7 +166,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + ACC + b); };
-    const uint32_t sumsf_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
+    constexpr int RS = Cfg::RAW_STAGES;
+    auto rawf_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + 2 * ACC + r); };
+    auto rawe_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + 2 * ACC + RS + r); };
+    const uint32_t sumsf_bar = bar0 + 8u * (2 * STAGES + 2 * ACC + 2 * RS);
     const uint32_t sumse_bar = sumsf_bar + 8u;
     const uint32_t drain_bar = sumse_bar + 8u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARRIERS);
@@ -189,11 +192,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 2 * Cfg::EPI_WARPS);
         }
+        for (int r = 0; r < RS; ++r) {
+            mbar_init(rawf_bar(r), 1);
+            mbar_init(rawe_bar(r), Cfg::XF_WARPS);
+        }
         mbar_init(sumsf_bar, 2 * Cfg::XF_WARPS);
         mbar_init(sumse_bar, 2 * Cfg::EPI_WARPS);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
     }
     if (warp == 0) tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
     tc_fence_before();
@@ -247,6 +256,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1
             tc_commit_pair(drain_bar, 0x1);
             bounded_wait(drain_bar, 0u, nullptr, p.ctl, kSiteS4DrainMma);
         }
+    } else if (warp == Cfg::PROD_WARP) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            Ring<RS> rr;
+            uint32_t armed = 0, armed_phase = 0;
+            const uint64_t pol = l2_policy_evict_normal();
+            bool ok = true;
+            for (int t = pair; ok && t < ntiles; t += npairs) {
+                int mb, nb;
+                tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
+                const int arow = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM;
+                const int brow = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!bounded_wait(rawe_bar(rr.slot()), rr.parity() ^ 1u, abort_flag, p.ctl, kSiteS4Prod)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(rawf_bar(rr.slot()), Cfg::RAW_BYTES);
+                    armed |= 1u << rr.slot();
+                    armed_phase = (armed_phase & ~(1u << rr.slot())) | (rr.parity() << rr.slot());
+                    uint8_t* dst = sRaw + rr.slot() * Cfg::RAW_BYTES;
+                    // 64 packed bytes of each row (k = 128 kb ... 128 kb + 127); rows
+                    // and bytes past the matrix are filled with zeros
+                    tma_load_2d(smem_u32(dst), &tmA, kb * Cfg::RAW_ROW, arow, rawf_bar(rr.slot()), pol);
+                    tma_load_2d(smem_u32(dst + Cfg::RAW_A_BYTES), &tmB, kb * Cfg::RAW_ROW, brow,
+                                rawf_bar(rr.slot()), pol);
+                    rr.next();
+                }
+            }
+            if (!ok)
+                for (int r = 0; r < RS; ++r)
+                    if (armed & (1u << r))
+                        bounded_wait(rawf_bar(r), (armed_phase >> r) & 1u, nullptr, p.ctl, kSiteS4Drain);
+        }
     } else if (warp < Cfg::SIG_WARP) {
         // ---------------------------------------------------- transform (both CTAs)
         // Thread x: quarter q (16 packed bytes = 32 values) of row slot rs;
@@ -256,98 +299,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(S4RawCfg::THREADS, 1
         const uint32_t peer_rb = mapa_shared(smem_u32(sRB), rank ^ 1u);
         const uint32_t peer_sumsf = mapa_shared(sumsf_bar, rank ^ 1u);
         Ring<STAGES> ps;
+        Ring<RS> rr;
         uint32_t sums_lap = 0;
         int signaled = 0;  // stages this thread has arrived on (the signaler counts on all)
-        bool ok = true;
-
-        // source of task i (A rows first) of a tile, and whether it is inside
-        // the matrix (rows past the end are read as zero bytes, never used)
-        struct Src {
-            const uint8_t* ptr;
-            bool valid;
-        };
-        auto task_src = [&](int t, int i) -> Src {
-            int mb, nb;
-            tile_coords(t, num_m, num_n, mb, nb, kGroupMPairs);
-            if (i < Cfg::A_TASKS) {
-                const int row = mb * 2 * Cfg::BM + static_cast<int>(rank) * Cfg::BM + rs + Cfg::ROW_SLOTS * i;
-                return {p.A + static_cast<int64_t>(row < p.M ? row : 0) * p.lda + 16 * q, row < p.M};
-            }
-            const int row = nb * Cfg::BN + static_cast<int>(rank) * Cfg::B_ROWS + rs +
-                            Cfg::ROW_SLOTS * (i - Cfg::A_TASKS);
-            return {p.B + static_cast<int64_t>(row < p.N ? row : 0) * p.ldb + 16 * q, row < p.N};
-        };
-        // DEPTH stages of loads in flight: the stage being converted and the
-        // DEPTH - 1 after it
-        Src src[Cfg::TASKS];
         int32_t rsum[Cfg::TASKS];
-        // Unconditional loads (a chunk past the end of K reads the row's first
-        // chunk instead and is zeroed when converted; rows past the end read
-        // row 0 and produce outputs nobody stores): a load whose value had to
-        // be selected against zero at issue would make the thread wait for it
-        // there, and the prefetch would stop overlapping.
-        auto issue = [&](uint4 (&dst)[Cfg::TASKS], int kb) {
-            const int off = kb * Cfg::RAW_ROW;  // byte offset of this stage's segment
-            const int o = off + 16 * q < kbytes ? off : 0;
-#pragma unroll
-            for (int i = 0; i < Cfg::TASKS; ++i) dst[i] = ld_raw16(src[i].ptr + o);
-        };
-        // converts the loaded stage kb into ring slot ps and signals the MMA;
-        // first issues the loads of stage kb_next into `nxt` (the buffer that
-        // stage kb - 1 used)
-        auto stage = [&](uint4 (&cur)[Cfg::TASKS], uint4 (&nxt)[Cfg::TASKS], int kb, int kb_next) -> bool {
-            if (kb_next < p.num_kb) issue(nxt, kb_next);
-            const bool inside = kb * Cfg::RAW_ROW + 16 * q < kbytes;
-            const bool got = bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
-                                          kSiteS4XfEmpty);
-            if (!__all_sync(0xffffffffu, got)) return false;
-#pragma unroll
-            for (int i = 0; i < Cfg::TASKS; ++i) {
-                const uint4 w = cur[i];
-                uint32_t e0, o0, e1, o1, e2, o2, e3, o3;
-                split_offset(w.x, e0, o0);
-                split_offset(w.y, e1, o1);
-                split_offset(w.z, e2, o2);
-                split_offset(w.w, e3, o3);
-                if (inside) {
-                    const uint32_t bytes = (e0 + o0) + (e1 + o1) + (e2 + o2) + (e3 + o3);  // <= 120 each
-                    rsum[i] = static_cast<int32_t>(__dp4a(bytes, 0x01010101u, static_cast<uint32_t>(rsum[i])));
-                } else {
-                    // past the end of K: zero products, nothing in the sums
-                    e0 = o0 = e1 = o1 = e2 = o2 = e3 = o3 = 0u;
-                }
-                const int r = rs + Cfg::ROW_SLOTS * (i < Cfg::A_TASKS ? i : i - Cfg::A_TASKS);
-                uint8_t* base = (i < Cfg::A_TASKS) ? sA + ps.slot() * Cfg::A_BYTES : sB + ps.slot() * Cfg::B_BYTES;
-                // 32 output bytes = 16-byte chunks 2q and 2q + 1 of the 128-byte
-                // row r, placed by the 128-byte swizzle (chunk c at c ^ (r & 7))
-                uint8_t* row = base + r * 128;
-                *reinterpret_cast<uint4*>(row + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(e0, o0, e1, o1);
-                *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (r & 7)) << 4)) = make_uint4(e2, o2, e3, o3);
-            }
-            fence_proxy_async_smem();
-            named_bar_arrive(1 + ps.slot(), Cfg::XF_THREADS + 32);
-            ps.next();
-            ++signaled;
-            return true;
-        };
-        constexpr int D = Cfg::DEPTH;
-        uint4 buf[D][Cfg::TASKS];  // indexed by compile-time constants only (unrolled)
+        bool ok = true;
         for (int t = pair; ok && t < ntiles; t += npairs) {
 #pragma unroll
-            for (int i = 0; i < Cfg::TASKS; ++i) {
-                src[i] = task_src(t, i);
-                rsum[i] = 0;
-            }
-#pragma unroll
-            for (int d = 0; d + 1 < D; ++d)
-                if (d < p.num_kb) issue(buf[d], d);
-            for (int kb0 = 0; ok && kb0 < p.num_kb; kb0 += D) {
-#pragma unroll
-                for (int d = 0; d < D; ++d) {
-                    const int kb = kb0 + d;
-                    if (!ok || kb >= p.num_kb) break;
-                    ok = stage(buf[d], buf[(d + D - 1) % D], kb, kb + D - 1);
+            for (int i = 0; i < Cfg::TASKS; ++i) rsum[i] = 0;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                bool got = bounded_wait(rawf_bar(rr.slot()), rr.parity(), abort_flag, p.ctl, kSiteS4XfRaw);
+                if (got) got = bounded_wait(empty_bar(ps.slot()), ps.parity() ^ 1u, abort_flag, p.ctl,
+                                            kSiteS4XfEmpty);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
                 }
+                const bool inside = kb * Cfg::RAW_ROW + 16 * q < kbytes;
+                const uint8_t* raw = sRaw + rr.slot() * Cfg::RAW_BYTES;
+                uint4 w[Cfg::TASKS];
+#pragma unroll
+                for (int i = 0; i < Cfg::TASKS; ++i) {
+                    const int r = rs + Cfg::ROW_SLOTS * (i < Cfg::A_TASKS ? i : i - Cfg::A_TASKS);
+                    const uint8_t* src = raw + (i < Cfg::A_TASKS ? 0 : Cfg::RAW_A_BYTES) + r * Cfg::RAW_ROW + 16 * q;
+                    w[i] = *reinterpret_cast<const uint4*>(src);
+                }
+#pragma unroll
+                for (int i = 0; i < Cfg::TASKS; ++i) {
+                    uint32_t e0, o0, e1, o1, e2, o2, e3, o3;
+                    split_offset(w[i].x, e0, o0);
+                    split_offset(w[i].y, e1, o1);
+                    split_offset(w[i].z, e2, o2);
+                    split_offset(w[i].w, e3, o3);
+                    if (inside) {
+                        const uint32_t bytes = (e0 + o0) + (e1 + o1) + (e2 + o2) + (e3 + o3);  // <= 120 each
+                        rsum[i] = static_cast<int32_t>(__dp4a(bytes, 0x01010101u, static_cast<uint32_t>(rsum[i])));
+                    } else {
+                        // past the end of K: zero products, nothing in the sums
+                        e0 = o0 = e1 = o1 = e2 = o2 = e3 = o3 = 0u;
+                    }
+                    const int r = rs + Cfg::ROW_SLOTS * (i < Cfg::A_TASKS ? i : i - Cfg::A_TASKS);
+                    uint8_t* base = (i < Cfg::A_TASKS) ? sA + ps.slot() * Cfg::A_BYTES : sB + ps.slot() * Cfg::B_BYTES;
+                    // 32 output bytes = 16-byte chunks 2q and 2q + 1 of the 128-byte
+                    // row r, placed by the 128-byte swizzle (chunk c at c ^ (r & 7))
+                    uint8_t* row = base + r * 128;
+                    *reinterpret_cast<uint4*>(row + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(e0, o0, e1, o1);
+                    *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (r & 7)) << 4)) = make_uint4(e2, o2, e3, o3);
+                }
+                // the packed bytes have been used: the producer may refill the slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rawe_bar(rr.slot()));
+                rr.next();
+                fence_proxy_async_smem();
+                named_bar_arrive(1 + ps.slot(), Cfg::XF_THREADS + 32);
+                ps.next();
+                ++signaled;
             }
             if (!ok) break;
             // row sums of this tile: the four quarters of a row are lanes 4j..4j+3
