@@ -75,11 +75,15 @@ FLOORS = {
 SWEEP_N = (512, 1024, 2048, 4096)
 
 # One-knob ablations (--ablate NAME): the library setter, the values tried
-# (the default first) and the ops whose speed the knob can change.
+# (the default first) and the ops whose speed the knob can change.  The
+# W4A16 rotations are CUDA graphs: a knob that changes the kernels they
+# launch re-captures them.
+RECAPTURE_W16 = ("pdl", "w4a16_tc")
 ABLATIONS = {
     "gemm_path": ("qg_set_gemm_path", (0, 1, 2), ("s8", "s4", "f16", "w4a4_gemm")),
     "w4a4_tile": ("qg_set_w4a4_pair_form", (0, 1), ("w4a4_gemm",)),
     "pdl": ("qg_set_pdl", (1, 0), ("w4a16", "w4a16_m16", "w4a16_m128")),
+    "w4a16_tc": ("qg_set_w4a16_tc_form", (0, 1), ("w4a16_m128",)),
     "s8_chunk": ("qg_set_s8_chunk", (16, 8, 4), ("s8",)),
     "l2_policy": ("qg_set_l2_policy", (0, 1, 2), ("s8", "s4", "f16")),
 }
@@ -526,7 +530,7 @@ def run_ablation(args, local_rank):
     try:
         for v in values:
             assert getattr(qg.lib(), setter)(v) == qg.QG_OK
-            if args.ablate == "pdl":
+            if args.ablate in RECAPTURE_W16:
                 wl.capture_w16()
             ev = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(args.steps)] for op in ops}
@@ -545,7 +549,7 @@ def run_ablation(args, local_rank):
                               "steps": args.steps, "op_ms_median": {op: round(t, 4) for op, t in med.items()}}))
     finally:
         getattr(qg.lib(), setter)(values[0])
-        if args.ablate == "pdl":
+        if args.ablate in RECAPTURE_W16:
             wl.capture_w16()
 
 

@@ -75,6 +75,7 @@ SIGNATURES = {
     "qg_set_w4a4_pair_form": (_int, [_int]),
     "qg_set_l2_policy": (_int, [_int]),
     "qg_set_pdl": (_int, [_int]),
+    "qg_set_w4a16_tc_form": (_int, [_int]),
     "qg_set_profile_events": (_int, [_p, _p]),
     "qgemm_s8": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p, _sz, _p]),
     "qgemm_s8_noalloc": (_int, [_i64, _i64, _i64, _p, _i64, _int, _p, _i64, _int, _p, _i64, _p]),

@@ -888,6 +888,7 @@ __global__ void __launch_bounds__(kD2Threads, 2)
 }
 
 static std::atomic<int> g_w4a16_pdl{1};
+static std::atomic<int> g_w4a16_tc_form{0};  // 0: resident weights where they fit, 1: ring only
 
 template <int MT, int NT>
 static int launch_w4a16(int M, int N, int K, const __half* X, int64_t ldx, const uint8_t* Wq,
@@ -1031,18 +1032,18 @@ static int launch_w4a16_gemv16(int M, int N, int K, const __half* X, int64_t ldx
 
 namespace qg {
 
-// Launches w4a16_tc_kernel for batch rows [m0, m0 + 128).
+// Launches w4a16_tc_kernel<Cfg> for batch rows [m0, m0 + 128).
+template <class Cfg>
 static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M, int N, int K, int m0,
                            const __half* S, __half* Y, int64_t ldy, const Ctl& ctl, int dev,
                            cudaStream_t s) {
-    using Cfg = W16TcCfg;
     static std::mutex mu;
     static bool attr_set[64] = {};
     {
         std::lock_guard<std::mutex> g(mu);
         if (!attr_set[dev]) {
             const cudaError_t e = cudaFuncSetAttribute(
-                w4a16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+                w4a16_tc_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
             if (e != cudaSuccess) return map_cuda(e);
             attr_set[dev] = true;
         }
@@ -1068,7 +1069,7 @@ static int launch_w4a16_tc(const CUtensorMap& tmX, const CUtensorMap& tmW, int M
     attr[0].val.programmaticStreamSerializationAllowed = g_w4a16_pdl.load() ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return map_cuda(cudaLaunchKernelEx(&cfg, w4a16_tc_kernel, tmX, tmW, p));
+    return map_cuda(cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<Cfg>, tmX, tmW, p));
 }
 
 // Resource budgets of the instances launched above.  The GEMV kernels count
@@ -1092,8 +1093,10 @@ QG_W16_BUDGET((k_w4a16_gemv16<2, 0>), "k_w4a16_gemv16<2,0>", kD2Threads, static_
 QG_W16_BUDGET((k_w4a16_gemv16<1, 4>), "k_w4a16_gemv16<1,4>", kD2Threads, static_cast<int>(kD1Budget), 2);
 QG_W16_BUDGET((k_w4a16_gemv16<1, 0>), "k_w4a16_gemv16<1,0>", kD2Threads, static_cast<int>(kD1Budget), 2);
 #undef QG_W16_BUDGET
-QG_KERNEL_BUDGET("w4a16_tc_kernel", reinterpret_cast<const void*>(w4a16_tc_kernel), W16TcCfg::THREADS,
-                 W16TcCfg::SMEM_BYTES, W16TcCfg::TMEM_COLS, W16TcCfg::KSPLIT, 1);
+QG_KERNEL_BUDGET("w4a16_tc_kernel<W16TcCfg>", reinterpret_cast<const void*>(w4a16_tc_kernel<W16TcCfg>),
+                 W16TcCfg::THREADS, W16TcCfg::SMEM_BYTES, W16TcCfg::TMEM_COLS, W16TcCfg::KSPLIT, 1);
+QG_KERNEL_BUDGET("w4a16_tc_kernel<W16TcResCfg>", reinterpret_cast<const void*>(w4a16_tc_kernel<W16TcResCfg>),
+                 W16TcResCfg::THREADS, W16TcResCfg::SMEM_BYTES, W16TcResCfg::TMEM_COLS, W16TcResCfg::KSPLIT, 1);
 
 }  // namespace qg
 
@@ -1103,6 +1106,12 @@ extern "C" {
 
 int qg_set_pdl(int enable) {
     g_w4a16_pdl.store(enable ? 1 : 0);
+    return QG_OK;
+}
+
+int qg_set_w4a16_tc_form(int form) {
+    if (form != 0 && form != 1) return QG_ERR_INVALID_ARG;
+    g_w4a16_tc_form.store(form);
     return QG_OK;
 }
 
@@ -1170,9 +1179,14 @@ int w4a16_gemm(int64_t M, int64_t N, int64_t K, const uint16_t* X, int64_t ldx, 
                               W16TcCfg::BM, CU_TENSOR_MAP_SWIZZLE_128B);
         if (!rc) rc = make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, K / 2, N, K / 2,
                                    W16TcCfg::BK / 2, W16TcCfg::BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+        // all packed rows of a K quarter resident when it holds <= 8 groups
+        const bool res = g_w4a16_tc_form.load() == 0 &&
+                         (K / kGroup + W16TcCfg::KSPLIT - 1) / W16TcCfg::KSPLIT <= W16TcResCfg::MAX_SLICE_GROUPS;
         for (int64_t r0 = 0; !rc && r0 < M; r0 += W16TcCfg::BM)
-            rc = launch_w4a16_tc(tmX, tmW, static_cast<int>(M), n, k, static_cast<int>(r0), Sh, Yh, ldy,
-                                 ctl, dev, s);
+            rc = res ? launch_w4a16_tc<W16TcResCfg>(tmX, tmW, static_cast<int>(M), n, k, static_cast<int>(r0),
+                                                    Sh, Yh, ldy, ctl, dev, s)
+                     : launch_w4a16_tc<W16TcCfg>(tmX, tmW, static_cast<int>(M), n, k, static_cast<int>(r0), Sh,
+                                                 Yh, ldy, ctl, dev, s);
         return rc;
     }
     // Rows are processed in chunks of up to 128 (8 m16 tiles per CTA).

@@ -60,27 +60,46 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32
         : "memory");
 }
 
-struct W16TcCfg {
+// WRES: the CTA's packed weights stay resident.  When a K quarter holds at
+// most 8 groups (K <= 4096) all of its packed rows (64 KB) are bulk-loaded
+// before the programmatic dependent wait, each 64-wide stage on a barrier of
+// its own, so the transform never waits on a refill and the first B slots
+// are dequantized before X (the previous kernel's output) may be read; only
+// X streams through the ring.  Otherwise X and the packed rows share one
+// ring, refilled as the MMA frees it.
+template <bool WRES_, int STAGES_, int BSLOTS_, int MAXG_, int SUB_>
+struct W16TcCfgT {
+    static constexpr bool WRES = WRES_;
     static constexpr int KSPLIT = 4;                    // CTAs per cluster, one K quarter each
     static constexpr int BM = 128;                      // batch rows per launch
     static constexpr int BN = 128;                      // weight rows (output columns) per cluster
-    static constexpr int BK = 64;                       // K per stage: 128 bytes of fp16
-    static constexpr int X_BYTES = BM * BK * 2;         // 16 KB
+    static constexpr int BK = 64;                       // K per sub-tile: 128 bytes of fp16
+    // 64-wide sub-tiles per ring stage: a stage's MMAs (4 per sub-tile) share
+    // one pair of barrier waits and one commit, which cost the issuing
+    // thread more than the MMAs themselves
+    static constexpr int SUB = SUB_;
+    static constexpr int X_SUB = BM * BK * 2;           // 16 KB
     static constexpr int B_ROWS = BN;                   // q * s rows
-    static constexpr int B_BYTES = B_ROWS * BK * 2;     // 16 KB fp16 operand
-    static constexpr int W_BYTES = BN * BK / 2;         // 4 KB packed nibbles
-    static constexpr int STAGES = 8;                    // X + packed-weight ring (memory latency)
-    static constexpr int BSLOTS = 3;                    // B operand ring (transform -> MMA)
+    static constexpr int B_SUB = B_ROWS * BK * 2;       // 16 KB fp16 operand
+    static constexpr int W_SUB = BN * BK / 2;           // 4 KB packed nibbles
+    static constexpr int X_BYTES = SUB * X_SUB, B_BYTES = SUB * B_SUB, W_BYTES = SUB * W_SUB;
+    static constexpr int STAGES = STAGES_;              // X (+ packed-weight) ring (memory latency)
+    static constexpr int BSLOTS = BSLOTS_;              // B operand ring (transform -> MMA)
+    static constexpr int MAX_SLICE_GROUPS = MAXG_;         // K groups per quarter
+    static constexpr int W_SLOTS = WRES ? 2 * MAX_SLICE_GROUPS / SUB : STAGES;  // packed stages held
+    // X and B rings of one depth move together: one commit per stage frees
+    // both slots (each tcgen05.commit costs the issuing thread about as much
+    // as three of the stage's MMAs)
+    static constexpr bool ONE_FREE = STAGES == BSLOTS;
     static constexpr int XFORM_WARPS = 16;
     static constexpr int XFORM_GROUPS = 2;              // groups of warps on alternate stages
     static constexpr int GROUP_WARPS = XFORM_WARPS / XFORM_GROUPS;
     static constexpr int THREADS = 32 * (2 + XFORM_WARPS);  // producer, MMA, transform/epilogue
     static constexpr int TMEM_COLS = 128;
-    static constexpr int MAX_SLICE_GROUPS = 64;         // K groups per quarter: K <= 32768
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * BSLOTS + 2;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SCALE_BYTES = BN * MAX_SLICE_GROUPS * 2;  // 16 KB
-    static constexpr int RING_BYTES = STAGES * (X_BYTES + W_BYTES) + BSLOTS * B_BYTES;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 * BSLOTS + 2 + (WRES ? W_SLOTS : 0);
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SCALE_BYTES = BN * MAX_SLICE_GROUPS * 2;
+    static constexpr int RING_BYTES = STAGES * X_BYTES + W_SLOTS * W_BYTES + BSLOTS * B_BYTES;
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + SCALE_BYTES + 1024;
     static constexpr int RED_STRIDE = BN + 4;           // floats per partial-tile row (bank spread)
     static constexpr int SLICE_ROWS = BM / KSPLIT;      // output rows each CTA finishes
@@ -88,13 +107,16 @@ struct W16TcCfg {
     static constexpr int RX_OFF = (BM * RED_STRIDE * 4 + 1023) / 1024 * 1024;  // received partials
     static constexpr uint32_t IDESC = make_idesc(0u, 0u, BM, B_ROWS);
 
-    static_assert(X_BYTES % 1024 == 0 && B_BYTES % 1024 == 0,
+    static_assert(X_SUB % 1024 == 0 && B_SUB % 1024 == 0,
                   "swizzle atoms need 1 KB alignment");
+    static_assert(SUB == 1 || SUB == 2, "a stage is one or two 64-wide sub-tiles (at most one K group)");
     static_assert(NUM_BARRIERS * 8 + 16 <= BAR_BYTES, "barrier area too small");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget exceeded");
     static_assert(RX_OFF + KSPLIT * SLICE_BYTES <= RING_BYTES, "partial tiles reuse the rings");
     static_assert(SLICE_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
+using W16TcCfg = W16TcCfgT<false, 8, 3, 64, 1>;    // any K up to 32768
+using W16TcResCfg = W16TcCfgT<true, 2, 2, 8, 2>;   // K <= 4096: 128-wide stages
 
 struct W16TcParams {
     int M, N, K;
@@ -114,10 +136,10 @@ enum W16TcSite : int {
     kSiteW16TcRx = 316,
 };
 
-__global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16TcCfg::THREADS, 1)
+template <class Cfg>
+__global__ void __cluster_dims__(Cfg::KSPLIT, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const W16TcParams p) {
-    using Cfg = W16TcCfg;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -125,17 +147,20 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
     constexpr int NB = Cfg::BSLOTS;
     uint8_t* sX = smem;                                   // S x 16 KB
     uint8_t* sB = sX + S * Cfg::X_BYTES;                  // NB x 32 KB
-    uint8_t* sW = sB + NB * Cfg::B_BYTES;                 // S x 4 KB
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + S * Cfg::W_BYTES);
+    uint8_t* sW = sB + NB * Cfg::B_BYTES;                 // W_SLOTS x 4 KB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + Cfg::W_SLOTS * Cfg::W_BYTES);
     unsigned short* sS = reinterpret_cast<unsigned short*>(reinterpret_cast<uint8_t*>(bars) + Cfg::BAR_BYTES);
     float* red = reinterpret_cast<float*>(smem);          // partial tile, after the K loop
     const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };             // X + W of stage s landed
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };             // X (+ W) of stage s landed
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };      // MMA done with stage s
     auto ready_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };  // B slot b written
-    auto bfree_bar = [&](int b) { return bar0 + 8u * (2 * S + NB + b); };  // MMA done with B slot b
+    auto bfree_bar = [&](int b) {  // MMA done with B slot b
+        return Cfg::ONE_FREE ? empty_bar(b) : bar0 + 8u * (2 * S + NB + b);
+    };
     const uint32_t accf_bar = bar0 + 8u * (2 * S + 2 * NB);
     const uint32_t rx_bar = bar0 + 8u * (2 * S + 2 * NB + 1);  // partials of this CTA's rows arrived
+    auto wfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * NB + 2 + i); };  // WRES: packed stage i
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -146,8 +171,8 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
     const int gq = (G + Cfg::KSPLIT - 1) / Cfg::KSPLIT;   // groups per quarter
     const int g_beg = min(G, static_cast<int>(rank) * gq), g_end = min(G, g_beg + gq);
     const int ng = g_end - g_beg;
-    const int num_kb = 2 * ng;                            // 64-wide stages of this quarter
-    const int kb0 = 2 * g_beg;                            // first global stage
+    const int num_kb = 2 * ng / Cfg::SUB;                 // ring stages of this quarter
+    const int kb0 = 2 * g_beg;                            // first global 64-wide sub-tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -156,10 +181,12 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(ready_bar(b), Cfg::GROUP_WARPS);  // one group transforms a stage
-            mbar_init(bfree_bar(b), 1);
+            if constexpr (!Cfg::ONE_FREE) mbar_init(bfree_bar(b), 1);
         }
         mbar_init(accf_bar, 1);
         mbar_init(rx_bar, 1);
+        if constexpr (Cfg::WRES)
+            for (int i = 0; i < Cfg::W_SLOTS; ++i) mbar_init(wfull_bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmX);
@@ -179,18 +206,32 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             const int pre = num_kb < S ? num_kb : S;
-            for (int i = 0; i < pre; ++i) {  // weights of the first stages before the wait
-                mbar_arrive_expect_tx(full_bar(i), Cfg::X_BYTES + Cfg::W_BYTES);
-                tma_load_2d(smem_u32(sW + i * Cfg::W_BYTES), &tmW, (kb0 + i) * (Cfg::BK / 2), n0,
-                            full_bar(i), pol_w);
+            constexpr uint32_t kStageTx = Cfg::WRES ? Cfg::X_BYTES : Cfg::X_BYTES + Cfg::W_BYTES;
+            if constexpr (Cfg::WRES) {
+                for (int i = 0; i < num_kb; ++i) {  // every packed stage, before the wait
+                    mbar_arrive_expect_tx(wfull_bar(i), Cfg::W_BYTES);
+                    for (int h = 0; h < Cfg::SUB; ++h)
+                        tma_load_2d(smem_u32(sW + i * Cfg::W_BYTES + h * Cfg::W_SUB), &tmW,
+                                    (kb0 + Cfg::SUB * i + h) * (Cfg::BK / 2), n0, wfull_bar(i), pol_w);
+                }
+            } else {
+                for (int i = 0; i < pre; ++i) {  // weights of the first stages before the wait
+                    mbar_arrive_expect_tx(full_bar(i), kStageTx);
+                    for (int h = 0; h < Cfg::SUB; ++h)
+                        tma_load_2d(smem_u32(sW + i * Cfg::W_BYTES + h * Cfg::W_SUB), &tmW,
+                                    (kb0 + Cfg::SUB * i + h) * (Cfg::BK / 2), n0, full_bar(i), pol_w);
+                }
             }
             pdl_wait_prior_grid();  // X may be the previous kernel's output
             // the previous kernel wrote X with ordinary stores; these loads
             // are TMA (async proxy) reads
             asm volatile("fence.proxy.async.global;" ::: "memory");
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem_u32(sX + i * Cfg::X_BYTES), &tmX, (kb0 + i) * Cfg::BK, p.m0, full_bar(i),
-                            pol_x);
+            for (int i = 0; i < pre; ++i) {
+                if constexpr (Cfg::WRES) mbar_arrive_expect_tx(full_bar(i), kStageTx);
+                for (int h = 0; h < Cfg::SUB; ++h)
+                    tma_load_2d(smem_u32(sX + i * Cfg::X_BYTES + h * Cfg::X_SUB), &tmX,
+                                (kb0 + Cfg::SUB * i + h) * Cfg::BK, p.m0, full_bar(i), pol_x);
+            }
             for (int i = pre; i < num_kb; ++i) {
                 const int s = i % S;
                 const uint32_t ph = static_cast<uint32_t>(i / S - 1) & 1u;  // round just finished
@@ -198,11 +239,15 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(full_bar(s), Cfg::X_BYTES + Cfg::W_BYTES);
-                tma_load_2d(smem_u32(sW + s * Cfg::W_BYTES), &tmW, (kb0 + i) * (Cfg::BK / 2), n0,
-                            full_bar(s), pol_w);
-                tma_load_2d(smem_u32(sX + s * Cfg::X_BYTES), &tmX, (kb0 + i) * Cfg::BK, p.m0, full_bar(s),
-                            pol_x);
+                mbar_arrive_expect_tx(full_bar(s), kStageTx);
+                for (int h = 0; h < Cfg::SUB; ++h) {
+                    const int kb = kb0 + Cfg::SUB * i + h;
+                    if constexpr (!Cfg::WRES)
+                        tma_load_2d(smem_u32(sW + s * Cfg::W_BYTES + h * Cfg::W_SUB), &tmW, kb * (Cfg::BK / 2),
+                                    n0, full_bar(s), pol_w);
+                    tma_load_2d(smem_u32(sX + s * Cfg::X_BYTES + h * Cfg::X_SUB), &tmX, kb * Cfg::BK, p.m0,
+                                full_bar(s), pol_x);
+                }
             }
             if (!ok) {
                 // copies already issued get a fixed time to land before the
@@ -226,12 +271,14 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
                 const uint32_t xa = smem_u32(sX + s * Cfg::X_BYTES);
                 const uint32_t ba = smem_u32(sB + b * Cfg::B_BYTES);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tc_mma<MmaKind::F16>(tmem_base, smem_desc_sw128(xa + 32u * k),
-                                         smem_desc_sw128(ba + 32u * k), Cfg::IDESC,
+                for (int k = 0; k < 4 * Cfg::SUB; ++k) {
+                    const uint32_t kk = 32u * (k & 3);  // 16 values of K inside a 64-wide sub-tile
+                    tc_mma<MmaKind::F16>(tmem_base, smem_desc_sw128(xa + (k >> 2) * Cfg::X_SUB + kk),
+                                         smem_desc_sw128(ba + (k >> 2) * Cfg::B_SUB + kk), Cfg::IDESC,
                                          (i > 0 || k > 0) ? 1u : 0u);
+                }
                 tc_commit(empty_bar(s));
-                tc_commit(bfree_bar(b));
+                if constexpr (!Cfg::ONE_FREE) tc_commit(bfree_bar(b));
             }
             tc_commit(accf_bar);  // also when stopped early: lets the epilogue leave
         }
@@ -253,7 +300,8 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
             const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
             // the weights of stage i have landed and the MMA is done with the
             // B slot's previous contents (stage i - NB)
-            bool got = bounded_wait(full_bar(s), ph, abort_flag, p.ctl, kSiteW16TcXform);
+            bool got = Cfg::WRES ? bounded_wait(wfull_bar(i), 0u, abort_flag, p.ctl, kSiteW16TcXform)
+                                 : bounded_wait(full_bar(s), ph, abort_flag, p.ctl, kSiteW16TcXform);
             if (got && i >= NB)
                 got = bounded_wait(bfree_bar(b), static_cast<uint32_t>(i / NB - 1) & 1u, abort_flag, p.ctl,
                                    kSiteW16TcXform);
@@ -261,27 +309,32 @@ __global__ void __cluster_dims__(W16TcCfg::KSPLIT, 1, 1) __launch_bounds__(W16Tc
                 ok = false;
                 break;
             }
-            const uint4 wv = *reinterpret_cast<const uint4*>(sW + s * Cfg::W_BYTES + r * 32 + q * 16);
-            const __half sc = __ushort_as_half(sS[r * Cfg::MAX_SLICE_GROUPS + (i >> 1)]);
-            const __half2 s2 = __halves2half2(sc, sc);
-            uint8_t* bst = sB + b * Cfg::B_BYTES + bw;
-            const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+            const int wslot = Cfg::WRES ? i : s;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t pr[4];
-                dequant_word_fast(words[h], pr);  // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
-                const uint32_t nat[4] = {__byte_perm(pr[0], pr[1], 0x5410), __byte_perm(pr[2], pr[3], 0x5410),
-                                         __byte_perm(pr[0], pr[1], 0x7632), __byte_perm(pr[2], pr[3], 0x7632)};
-                uint32_t w[4];
+            for (int sub = 0; sub < Cfg::SUB; ++sub) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(sW + wslot * Cfg::W_BYTES + sub * Cfg::W_SUB +
+                                                                 r * 32 + q * 16);
+                const __half sc = __ushort_as_half(sS[r * Cfg::MAX_SLICE_GROUPS + ((Cfg::SUB * i + sub) >> 1)]);
+                const __half2 s2 = __halves2half2(sc, sc);
+                uint8_t* bst = sB + b * Cfg::B_BYTES + sub * Cfg::B_SUB + bw;
+                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __half2 qv = *reinterpret_cast<const __half2*>(&nat[j]);
-                    __half2 a = __hmul2(qv, s2);  // q * s, rounded to fp16
-                    w[j] = *reinterpret_cast<uint32_t*>(&a);
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pr[4];
+                    dequant_word_fast(words[h], pr);  // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
+                    const uint32_t nat[4] = {__byte_perm(pr[0], pr[1], 0x5410), __byte_perm(pr[2], pr[3], 0x5410),
+                                             __byte_perm(pr[0], pr[1], 0x7632), __byte_perm(pr[2], pr[3], 0x7632)};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const __half2 qv = *reinterpret_cast<const __half2*>(&nat[j]);
+                        __half2 a = __hmul2(qv, s2);  // q * s, rounded to fp16
+                        w[j] = *reinterpret_cast<uint32_t*>(&a);
+                    }
+                    const int c = 4 * q + h;  // 16-byte chunk: k = 8c .. 8c + 7
+                    const uint32_t off = static_cast<uint32_t>((c ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(bst + off) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                const int c = 4 * q + h;                   // 16-byte chunk: k = 8c .. 8c + 7
-                const uint32_t off = static_cast<uint32_t>((c ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(bst + off) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -200,6 +200,15 @@ int qg_set_l2_policy(int mode);
  * overlap off. */
 int qg_set_pdl(int enable);
 
+/* Form of the tensor-core w4a16_gemm kernel (batches above 16 rows):
+ *   0 = default: when a K quarter holds at most 8 groups (K <= 4096) every
+ *       packed weight row of a CTA's quarter is loaded before the dependency
+ *       wait and stays in shared memory, and only X streams through the ring;
+ *   1 = X and the packed rows share one ring at every K (the form used for
+ *       K > 4096).
+ * Both give identical bits.  QG_ERR_INVALID_ARG for another value. */
+int qg_set_w4a16_tc_form(int form);
+
 /* Measurement hook: while `before` and `after` are non-NULL cudaEvent_t
  * handles (created by the caller), every qgemm_s8, qgemm_s4, gemm_f16 and
  * w4a4_gemm call records `before` on its stream right before launching its

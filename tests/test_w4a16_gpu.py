@@ -80,7 +80,27 @@ def test_w4a16_group_scales_are_per_row_and_group(dev, oracle):
     assert_fp16_close(_run(dev, X, Wq, S), oracle.w4a16(X, Wq, S, GROUP), "w4a16 pow2 scales")
 
 
-@pytest.mark.parametrize("M", [1, 12, 32])
+@pytest.mark.parametrize("M,N,K", [(17, 260, 384), (130, 48, 256), (40, 72, 1024), (128, 4096, 4096),
+                                   (200, 520, 3968), (33, 128, 4224), (64, 256, 8192)])
+def test_w4a16_tc_forms_identical(dev, oracle, M, N, K):
+    """The tensor-core kernel with every packed row of a K quarter resident
+    (K <= 4096, the default there) and the ring form give the same bits;
+    K = 4224 and 8192 exceed the resident form and run the ring form both
+    times."""
+    import bit_quantized_tensor_gb300 as qg
+    X, Wq, S = _operands(M, N, K, idx=M + K)
+    try:
+        got = {}
+        for form in (0, 1):
+            assert qg.lib().qg_set_w4a16_tc_form(form) == qg.QG_OK
+            got[form] = _run(dev, X, Wq, S)
+    finally:
+        qg.lib().qg_set_w4a16_tc_form(0)
+    assert np.array_equal(got[0].view(np.uint16), got[1].view(np.uint16))
+    assert_fp16_close(got[0], oracle.w4a16(X, Wq, S, GROUP), f"w4a16 tc {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 12, 32, 128])
 @pytest.mark.parametrize("pdl", [1, 0])
 def test_w4a16_chain_reads_previous_output(dev, oracle, pdl, M):
     """Layer chain Y_i = f_i(Y_{i-1}) on one stream: with programmatic
