@@ -5,34 +5,39 @@
 // ("fused-int4-gemm-sm75" README: weight-only int4 with group-128 scales.)
 // A cluster of 4 CTAs owns 128 output columns (128 weight rows) for up to 128
 // batch rows and splits K four ways: CTA r handles a contiguous quarter of
-// the K groups.  Per 64-wide K stage a CTA
-//  - TMA-loads its 128 x 64 fp16 tile of X and its 128 rows x 32 bytes of
-//    packed weights into an 8-deep ring (every cluster re-reads X from L2,
-//    and a load took about 2000 cycles to land under that traffic);
+// the K groups.  Per K stage a CTA
+//  - TMA-loads its 128-row tile of X (and, in the ring form, the packed
+//    weight rows of the stage); in the resident form (a quarter of at most 8
+//    groups, K <= 4096) all packed rows of the quarter (64 KB) are loaded
+//    before the programmatic dependent wait and only X streams;
 //  - dequantizes in registers, as the SM75 page does: each weight becomes
 //    the fp16 product q * s (rounded once, at most 2^-11 of the weight); the
 //    128 rows go to the 128-byte-swizzled K-major layout of the MMA's B
-//    operand, in a ring of three slots (with two, the transform of a stage
-//    waited for the MMA two stages back to complete, which paced the loop).
-//    Two groups of eight warps take alternate stages: one warp's pass over a
+//    operand.  Groups of warps take alternate stages: one warp's pass over a
 //    stage is latency-bound (shared-memory loads, the proxy fence, the
 //    barrier arrival), so two stages in flight double the transform rate;
 //  - issues tcgen05.mma kind::f16 M=128 N=128 (one thread) into a 128-column
 //    TMEM accumulator.
-// The loop is bound by shared-memory traffic: per stage the ring takes X and
-// the packed rows, the transform writes the B operand and the MMA reads X and
-// B.  An exact alternative (q * s split into two exact fp16 rows, q * s_hi
-// and q * s_lo, with s_hi the scale with its three lowest mantissa bits
-// cleared) doubles the B operand, 104 KB of shared-memory traffic per stage
-// against 72 KB here, and was slower by that much.
+// What paces the loop (globaltimer traces of a chain of calls, M = 128,
+// N = K = 4096): one such MMA runs in about 30 ns, but each stage also costs
+// the issuing thread about 200 ns of barrier waits, fences and commits, so
+// the resident form takes 128-wide stages (8 MMAs and one commit each; the X
+// and B rings have one depth, so one commit frees both slots): 12.2 -> 10.6
+// us per call.  With MMAs skipped the transform alone takes about as long as
+// the loop now does.  An exact alternative to the rounded q * s (two exact
+// fp16 rows, q * s_hi and q * s_lo, with s_hi the scale with its three
+// lowest mantissa bits cleared) doubles the B operand and was slower by that.
 // At the end every CTA stores its 128 x 128 fp32
 // partial tile in shared memory and, once every CTA of the cluster is past
 // its K loop, bulk-copies rows [32 r, 32 r + 32) of it into CTA r's shared
 // memory (the copy engine signals CTA r's barrier with the byte count); CTA r
-// adds the four partials of its rows and stores them as fp16.  Both cluster
-// barriers are relaxed: the copies carry their own completion, and a barrier
-// with release semantics cost about half a microsecond here, as much as the
-// whole exchange.  Weight rows and scales are fetched before the
+// adds the four partials of its rows and stores them as fp16.  The copies
+// run at about 20 bytes per clock (1.4 us for 50 KB; 16-byte copies take
+// 0.26 us); sending the rows from registers with 16-byte st.async stores
+// (2.7 us) or plain remote stores and a release/acquire cluster barrier
+// (3.0 us) was slower.  Both cluster barriers are relaxed: the copies carry
+// their own completion, and a barrier with release semantics cost about half
+// a microsecond here.  Weight rows and scales are fetched before the
 // programmatic dependent wait; X after it.  Every wait is bounded.  Scales
 // must stay below 8188 in magnitude (8 * s must be a finite fp16).
 #pragma once
@@ -67,7 +72,7 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32
 // are dequantized before X (the previous kernel's output) may be read; only
 // X streams through the ring.  Otherwise X and the packed rows share one
 // ring, refilled as the MMA frees it.
-template <bool WRES_, int STAGES_, int BSLOTS_, int MAXG_, int SUB_>
+template <bool WRES_, int STAGES_, int BSLOTS_, int MAXG_, int SUB_, int XGROUPS_>
 struct W16TcCfgT {
     static constexpr bool WRES = WRES_;
     static constexpr int KSPLIT = 4;                    // CTAs per cluster, one K quarter each
@@ -92,7 +97,7 @@ struct W16TcCfgT {
     // as three of the stage's MMAs)
     static constexpr bool ONE_FREE = STAGES == BSLOTS;
     static constexpr int XFORM_WARPS = 16;
-    static constexpr int XFORM_GROUPS = 2;              // groups of warps on alternate stages
+    static constexpr int XFORM_GROUPS = XGROUPS_;       // groups of warps on alternate stages
     static constexpr int GROUP_WARPS = XFORM_WARPS / XFORM_GROUPS;
     static constexpr int THREADS = 32 * (2 + XFORM_WARPS);  // producer, MMA, transform/epilogue
     static constexpr int TMEM_COLS = 128;
@@ -110,13 +115,16 @@ struct W16TcCfgT {
     static_assert(X_SUB % 1024 == 0 && B_SUB % 1024 == 0,
                   "swizzle atoms need 1 KB alignment");
     static_assert(SUB == 1 || SUB == 2, "a stage is one or two 64-wide sub-tiles (at most one K group)");
+    static constexpr int TPR = 32 * GROUP_WARPS / BN;   // transform threads per weight row
+    static constexpr int WPT = 8 / TPR;                 // packed 32-bit words per thread per sub-tile
+    static_assert(TPR * BN == 32 * GROUP_WARPS && (WPT == 2 || WPT == 4), "transform thread mapping");
     static_assert(NUM_BARRIERS * 8 + 16 <= BAR_BYTES, "barrier area too small");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget exceeded");
     static_assert(RX_OFF + KSPLIT * SLICE_BYTES <= RING_BYTES, "partial tiles reuse the rings");
     static_assert(SLICE_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
-using W16TcCfg = W16TcCfgT<false, 8, 3, 64, 1>;    // any K up to 32768
-using W16TcResCfg = W16TcCfgT<true, 2, 2, 8, 2>;   // K <= 4096: 128-wide stages
+using W16TcCfg = W16TcCfgT<false, 8, 3, 64, 1, 2>;    // any K up to 32768
+using W16TcResCfg = W16TcCfgT<true, 2, 2, 8, 2, 2>;   // K <= 4096: 128-wide stages
 
 struct W16TcParams {
     int M, N, K;
@@ -293,7 +301,7 @@ __global__ void __cluster_dims__(Cfg::KSPLIT, 1, 1) __launch_bounds__(Cfg::THREA
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::XFORM_WARPS) : "memory");
         const int grp = (warp - 2) / Cfg::GROUP_WARPS;    // stages grp, grp + 2, ...
         const int gt = tid - grp * 32 * Cfg::GROUP_WARPS;  // 0..255 within the group
-        const int r = gt >> 1, q = gt & 1;                // weight row, 32-value half of the stage
+        const int r = gt / Cfg::TPR, q = gt % Cfg::TPR;   // weight row, part of the row's 64 values
         const uint32_t bw = (r >> 3) * 1024 + (r & 7) * 128;  // row start in the swizzled B stage
         for (int i = grp; i < num_kb; i += Cfg::XFORM_GROUPS) {
             const int s = i % S, b = i % NB;
@@ -312,14 +320,20 @@ __global__ void __cluster_dims__(Cfg::KSPLIT, 1, 1) __launch_bounds__(Cfg::THREA
             const int wslot = Cfg::WRES ? i : s;
 #pragma unroll
             for (int sub = 0; sub < Cfg::SUB; ++sub) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(sW + wslot * Cfg::W_BYTES + sub * Cfg::W_SUB +
-                                                                 r * 32 + q * 16);
+                const uint8_t* wsrc = sW + wslot * Cfg::W_BYTES + sub * Cfg::W_SUB + r * 32 + q * 4 * Cfg::WPT;
+                uint32_t words[Cfg::WPT];
+                if constexpr (Cfg::WPT == 4) {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(wsrc);
+                    words[0] = wv.x, words[1] = wv.y, words[2] = wv.z, words[3] = wv.w;
+                } else {
+                    const uint2 wv = *reinterpret_cast<const uint2*>(wsrc);
+                    words[0] = wv.x, words[1] = wv.y;
+                }
                 const __half sc = __ushort_as_half(sS[r * Cfg::MAX_SLICE_GROUPS + ((Cfg::SUB * i + sub) >> 1)]);
                 const __half2 s2 = __halves2half2(sc, sc);
                 uint8_t* bst = sB + b * Cfg::B_BYTES + sub * Cfg::B_SUB + bw;
-                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 0; h < Cfg::WPT; ++h) {
                     uint32_t pr[4];
                     dequant_word_fast(words[h], pr);  // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
                     const uint32_t nat[4] = {__byte_perm(pr[0], pr[1], 0x5410), __byte_perm(pr[2], pr[3], 0x5410),
@@ -331,7 +345,7 @@ __global__ void __cluster_dims__(Cfg::KSPLIT, 1, 1) __launch_bounds__(Cfg::THREA
                         __half2 a = __hmul2(qv, s2);  // q * s, rounded to fp16
                         w[j] = *reinterpret_cast<uint32_t*>(&a);
                     }
-                    const int c = 4 * q + h;  // 16-byte chunk: k = 8c .. 8c + 7
+                    const int c = Cfg::WPT * q + h;  // 16-byte chunk: k = 8c .. 8c + 7
                     const uint32_t off = static_cast<uint32_t>((c ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4*>(bst + off) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
