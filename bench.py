@@ -67,7 +67,7 @@ FLOORS = {
     ("fp16_gemm_8192", "frac_of_f16_peak"): 0.77,
     ("w4a16_m1_4096", "frac_of_hbm"): 0.32,
     ("w4a16_m16_4096", "frac_of_hbm"): 0.18,
-    ("w4a16_m128_4096", "frac_of_hbm"): 0.10,
+    ("w4a16_m128_4096", "frac_of_hbm"): 0.13,
     ("w4a4_4096x8192x8192_r32", "frac_of_fp8_peak"): 0.16,
 }
 
