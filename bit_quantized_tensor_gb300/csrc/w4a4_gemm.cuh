@@ -353,6 +353,13 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                                 tmem_ld_16x256b_x2(taddr + (static_cast<uint32_t>(16 * hf) << 16) +
                                                        static_cast<uint32_t>(16 * (ch + 1)),
                                                    rb[(ch + 1) & 1][hf]);
+                        } else {
+                            // the buffer's last TMEM reads completed at the
+                            // previous tcgen05.wait::ld: hand it back before
+                            // the last chunk's arithmetic
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(acce_bar(as.slot()));
                         }
                         // c = sW * sX for the chunk's 2 column pairs and 4 rows, as
                         // packed pairs (both factors already paired in registers)
@@ -372,9 +379,6 @@ __global__ void __launch_bounds__(W4A4Cfg::THREADS, 1)
                         }
                         if (ch + 1 < NCH) tmem_wait_ld();
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(as.slot()));
                     as.next();
                 }
                 if (!ok) break;

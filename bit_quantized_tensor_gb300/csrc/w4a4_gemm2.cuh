@@ -341,6 +341,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                                 tmem_ld_16x256b_x1(taddr + (static_cast<uint32_t>(16 * hf) << 16) +
                                                        static_cast<uint32_t>(8 * (c + 1)),
                                                    rb[(c + 1) & 1][hf]);
+                        } else {
+                            // the buffer's last TMEM reads completed at the
+                            // previous tcgen05.wait::ld: hand it back before
+                            // the last group's arithmetic, with the arrival
+                            // only (no cluster-scope release needed)
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster_relaxed(lead_acce0 + 8u * as.slot());
                         }
                         const uint64_t w = *reinterpret_cast<const uint64_t*>(swc + 8 * c);
 #pragma unroll
@@ -355,11 +363,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                             }
                         if (c + 1 < NG) tmem_wait_ld();
                     }
-                    // The buffer's TMEM reads completed at tcgen05.wait::ld, so the
-                    // leader needs the arrival only, not a cluster-scope release.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(lead_acce0 + 8u * as.slot());
                     as.next();
                 }
                 if (!ok) break;
