@@ -599,6 +599,34 @@ def sweep_working_set(op: str, n: int) -> int:
     return 2 * 2 * n * n + 2 * n * n
 
 
+GRAPH_CALLS = 20
+
+
+def graph_ms_per_call(fn, stream, reps: int) -> float:
+    """Median over `reps` replays (timed on `stream`, the current stream) of
+    a CUDA graph of GRAPH_CALLS calls of `fn`, divided by GRAPH_CALLS (ms
+    per call)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):  # the library launches on the capture stream
+        for _ in range(GRAPH_CALLS):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(reps, 3)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / GRAPH_CALLS)
+    del g
+    return statistics.median(times)
+
+
 def measure_sweep(wl, stream, bf16: float, steps: int = 30, warmup: int = 3,
                   sizes=SWEEP_N) -> dict:
     """The square GEMMs at the sweep sizes: back to back (no flush), median
@@ -642,8 +670,12 @@ def measure_sweep(wl, stream, bf16: float, steps: int = 30, warmup: int = 3,
                 if i >= 0:
                     evs.append((a, b, ka, kb))
             torch.cuda.synchronize()
-            ms = statistics.median(a.elapsed_time(b) for a, b, _, _ in evs)
+            ms_call = statistics.median(a.elapsed_time(b) for a, b, _, _ in evs)
             kms = statistics.median(ka.elapsed_time(kb) for _, _, ka, kb in evs)
+            # The same calls replayed as a CUDA graph of GRAPH_CALLS back to
+            # back: per-call GPU time without the host's enqueue latency,
+            # which dominates a single small call timed from the host.
+            ms = graph_ms_per_call(fn, stream, steps)
             ops = 2.0 * n ** 3
             ws = sweep_working_set(op, n)
             out[f"{'int8' if op == 's8' else 'int4' if op == 's4' else 'fp16'}_{n}"] = {
@@ -651,7 +683,11 @@ def measure_sweep(wl, stream, bf16: float, steps: int = 30, warmup: int = 3,
                 "kernel_TOPS": round(ops / kms / 1e9, 1),
                 f"frac_of_{kind[op]}_peak": round(ops / ms / 1e9 / peak[op], 3),
                 f"kernel_frac_of_{kind[op]}_peak": round(ops / kms / 1e9 / peak[op], 3),
-                "us": round(ms * 1e3, 2), "working_set_bytes": ws,
+                "us": round(ms * 1e3, 2), "us_single_call": round(ms_call * 1e3, 2),
+                "working_set_bytes": ws,
+                "timing": f"us: a CUDA graph of {GRAPH_CALLS} back-to-back calls, per call; "
+                          "us_single_call: one call between events (host enqueue included); "
+                          "kernel_TOPS: the main kernel between library-recorded events of a single call",
                 "l2": "hot (working set fits in L2, back-to-back calls)" if ws <= l2
                       else "working set larger than L2 (back-to-back calls)"}
         del A8, B8, A4, B4, Af, Bf, C32, C16, ws8, ws4
