@@ -67,8 +67,8 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32
 
 // WRES: the CTA's packed weights stay resident.  When a K quarter holds at
 // most 8 groups (K <= 4096) all of its packed rows (64 KB) are bulk-loaded
-// before the programmatic dependent wait, each 64-wide stage on a barrier of
-// its own, so the transform never waits on a refill and the first B slots
+// before the programmatic dependent wait, each ring stage's rows on a barrier
+// of their own, so the transform never waits on a refill and the first B slots
 // are dequantized before X (the previous kernel's output) may be read; only
 // X streams through the ring.  Otherwise X and the packed rows share one
 // ring, refilled as the MMA frees it.
@@ -90,11 +90,11 @@ struct W16TcCfgT {
     static constexpr int X_BYTES = SUB * X_SUB, B_BYTES = SUB * B_SUB, W_BYTES = SUB * W_SUB;
     static constexpr int STAGES = STAGES_;              // X (+ packed-weight) ring (memory latency)
     static constexpr int BSLOTS = BSLOTS_;              // B operand ring (transform -> MMA)
-    static constexpr int MAX_SLICE_GROUPS = MAXG_;         // K groups per quarter
+    static constexpr int MAX_SLICE_GROUPS = MAXG_;      // K groups per quarter, at most
     static constexpr int W_SLOTS = WRES ? 2 * MAX_SLICE_GROUPS / SUB : STAGES;  // packed stages held
     // X and B rings of one depth move together: one commit per stage frees
-    // both slots (each tcgen05.commit costs the issuing thread about as much
-    // as three of the stage's MMAs)
+    // both slots (a tcgen05.commit costs the issuing thread about as much as
+    // an MMA: 30 ns)
     static constexpr bool ONE_FREE = STAGES == BSLOTS;
     static constexpr int XFORM_WARPS = 16;
     static constexpr int XFORM_GROUPS = XGROUPS_;       // groups of warps on alternate stages
