@@ -109,25 +109,24 @@ __device__ __forceinline__ void codes_exact(const float (&x)[16], float s, uint3
 __device__ __forceinline__ bool codes_fast(const float (&x)[16], float r, uint32_t (&grp)[4]) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     constexpr float kNearTie = 0.5f - 0x1p-17f;
-    bool near = false;
+    // the same IEEE operations on pairs of values (f32x2), and the largest
+    // |d| of the row compared once
+    const uint64_t r2 = pack_f32x2(r, r), magic2 = pack_f32x2(kMagic, kMagic);
+    float dmax = 0.f;
     uint32_t pair[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        uint32_t b[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float y = x[2 * p + e] * r;
-            const float tq = __fadd_rn(y, kMagic);
-            const float d = __fsub_rn(y, __fsub_rn(tq, kMagic));
-            near |= fabsf(d) > kNearTie;
-            b[e] = __float_as_uint(tq);
-        }
-        // low nibble <- b[0], high nibble <- b[1]
-        pair[p] = (b[0] & 0x0Fu) | ((b[1] << 4) & 0xF0u);
+        const uint64_t y = mul2(pack_f32x2(x[2 * p], x[2 * p + 1]), r2);
+        const uint64_t tq = add2(y, magic2);
+        const float2 d = unpack_f32x2(sub2(y, sub2(tq, magic2)));
+        dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
+        const float2 tf = unpack_f32x2(tq);
+        // low nibble <- the pair's first value, high nibble <- its second
+        pair[p] = (__float_as_uint(tf.x) & 0x0Fu) | ((__float_as_uint(tf.y) << 4) & 0xF0u);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) grp[c] = __byte_perm(pair[2 * c], pair[2 * c + 1], 0x0040);
-    return near;
+    return dmax > kNearTie;
 }
 
 __device__ __forceinline__ float absmax16(const float (&x)[16]) {
