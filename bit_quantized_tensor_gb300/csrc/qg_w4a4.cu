@@ -337,20 +337,33 @@ __global__ void __launch_bounds__(kQThreads, 2)
 // both the block-scaled product and the low-rank unit.  An fp16 scale times
 // an fp16 multiplier has at most 22 significant bits, so the fp32 product is
 // exact.
-__global__ void k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
-                                    const __half* __restrict__ S, const __half* __restrict__ alpha,
-                                    float* __restrict__ St) {
-    const int64_t total = static_cast<int64_t>(nblk + 1) * rows_p;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t j = i / rows_p;
-        const int64_t r = i - j * rows_p;
-        float v = 0.f;
-        if (r < rows) {
-            v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
-            if (alpha) v *= __half2float(alpha[r]);
+__global__ void __launch_bounds__(256) k_scales_transposed(int64_t rows, int64_t rows_p, int nblk,
+                                                          const __half* __restrict__ S,
+                                                          const __half* __restrict__ alpha,
+                                                          float* __restrict__ St) {
+    // 32 x 32 tiles through shared memory: a warp reads 32 consecutive
+    // blocks of one row and writes 32 consecutive rows of one block
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+    const int64_t rtiles = (rows_p + 31) / 32, jtiles = (nblk + 1 + 31) / 32;
+    for (int64_t t = blockIdx.x; t < rtiles * jtiles; t += gridDim.x) {
+        const int64_t r0 = (t % rtiles) * 32;
+        const int64_t j0 = (t / rtiles) * 32;
+        const int64_t j = j0 + tx;
+        for (int rr = ty; rr < 32; rr += 8) {
+            const int64_t r = r0 + rr;
+            float v = 0.f;
+            if (r < rows && j <= nblk) {
+                v = (j == nblk) ? 1.f : __half2float(S[r * nblk + j]);
+                if (alpha) v *= __half2float(alpha[r]);
+            }
+            tile[rr][tx] = v;
         }
-        St[i] = v;
+        __syncthreads();
+        const int64_t r = r0 + tx;
+        for (int jj = ty; jj < 32; jj += 8)
+            if (j0 + jj <= nblk && r < rows_p) St[(j0 + jj) * rows_p + r] = tile[tx][jj];
+        __syncthreads();
     }
 }
 
@@ -558,9 +571,9 @@ static int w4a4_gemm_impl(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, co
 
     int rc = s4_to_e4m3_pair(Xq, M, K / 2, A8, Wq, N, K / 2, B8, K, dev, s);
     if (rc) return rc;
-    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
+    k_scales_transposed<<<conv_grid(dev, 256 * ((nblk + 32) / 32) * ((Mp + 31) / 32)), 256, 0, s>>>(
         M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), nullptr, SXt);
-    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
+    k_scales_transposed<<<conv_grid(dev, 256 * ((nblk + 32) / 32) * ((Np + 31) / 32)), 256, 0, s>>>(
         N, Np, nblk, reinterpret_cast<const __half*>(Wscale), reinterpret_cast<const __half*>(alpha),
         SWt);
     rc = map_cuda(cudaGetLastError());
@@ -615,7 +628,7 @@ int w4a4_prepack_weights(int64_t N, int64_t K, const uint8_t* Wq, const uint16_t
     float* SWt = reinterpret_cast<float*>(B8 + w4a4_packed_scales_offset(N, K));
     int rc = s4_to_e4m3_rows(Wq, N, K / 2, B8, K, dev, s);
     if (rc) return rc;
-    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Np), 256, 0, s>>>(
+    k_scales_transposed<<<conv_grid(dev, 256 * ((nblk + 32) / 32) * ((Np + 31) / 32)), 256, 0, s>>>(
         N, Np, nblk, reinterpret_cast<const __half*>(Wscale), reinterpret_cast<const __half*>(alpha), SWt);
     return map_cuda(cudaGetLastError());
 }
@@ -649,7 +662,7 @@ int w4a4_gemm_prepacked(int64_t M, int64_t N, int64_t K, const uint8_t* Xq, cons
     float* SXt = reinterpret_cast<float*>(A8 + ((static_cast<size_t>(M) * K + 255) & ~static_cast<size_t>(255)));
     int rc = s4_to_e4m3_rows(Xq, M, K / 2, A8, K, dev, s);
     if (rc) return rc;
-    k_scales_transposed<<<conv_grid(dev, (nblk + 1) * Mp), 256, 0, s>>>(
+    k_scales_transposed<<<conv_grid(dev, 256 * ((nblk + 32) / 32) * ((Mp + 31) / 32)), 256, 0, s>>>(
         M, Mp, nblk, reinterpret_cast<const __half*>(Xscale), nullptr, SXt);
     rc = map_cuda(cudaGetLastError());
     if (rc) return rc;
